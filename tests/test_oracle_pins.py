@@ -1,0 +1,371 @@
+"""Pins of the CPU oracle against things other than itself.
+
+Each test checks one oracle function against a library routine, a
+hand-written table of the GGUF Q4_K format, a closed form, an invariant or a
+brute-force computation written independently here, chosen so that a plausible
+slip in the oracle (a dropped term, a wrong sign, a swapped index or byte)
+fails at least one of them.  CPU only.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import synthetic
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _read_table(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                rows.append(line.split())
+    return rows
+
+
+def _block(d_bits=0, dmin_bits=0, scales=None, qs=None):
+    b = np.zeros(144, dtype=np.uint8)
+    b[0], b[1] = d_bits & 255, d_bits >> 8
+    b[2], b[3] = dmin_bits & 255, dmin_bits >> 8
+    if scales is not None:
+        b[4:16] = np.asarray(scales, dtype=np.uint8)
+    if qs is not None:
+        b[16:144] = np.asarray(qs, dtype=np.uint8)
+    return b
+
+
+def _h(v):
+    """binary16 bits of a value exactly representable in fp16 (numpy)."""
+    return int(np.array([v], dtype="<f2").view(np.uint16)[0])
+
+
+# ------------------------------------------------------------------ fp16 ----
+
+def test_half_decode_exhaustive_against_numpy():
+    bits = np.arange(65536, dtype=np.uint16)
+    got = oracle.half_bits_to_double(bits)
+    want = bits.view(np.float16).astype(np.float64)
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+    # signed zeros keep their sign
+    assert math.copysign(1.0, got[0x8000]) == -1.0
+
+
+def test_float_to_half_rounding_against_numpy():
+    rng = np.random.Generator(np.random.PCG64(7))
+    parts = [
+        rng.standard_normal(200000).astype(np.float32),
+        (rng.standard_normal(200000) * 1e-5).astype(np.float32),  # fp16 subnormal range
+        (rng.standard_normal(50000) * 3e4).astype(np.float32),  # near overflow
+        rng.integers(0, 2**32, 200000, dtype=np.uint64).astype(np.uint32).view(np.float32),
+    ]
+    # exact ties between neighbouring fp16 values (normal and subnormal)
+    h = np.arange(0, 0x7bff, dtype=np.uint16)
+    lo = h.view(np.float16).astype(np.float64)
+    hi = (h + 1).view(np.float16).astype(np.float64)
+    parts.append(((lo + hi) / 2).astype(np.float32))
+    parts.append(np.array([65504.0, 65519.99, 65520.0, 1e9, np.inf, -np.inf, 0.0, -0.0,
+                           2.0**-25, 2.0**-25 * 1.0000001, 3 * 2.0**-25, 2.0**-24], dtype=np.float32))
+    f = np.concatenate(parts)
+    f = f[~np.isnan(f)]
+    got = oracle.float_to_half_bits(f)
+    with np.errstate(over="ignore"):
+        want = f.astype(np.float16).view(np.uint16)
+    assert np.array_equal(got, want)
+
+
+# ---------------------------------------------------------- block layout ----
+
+def test_scale_bits_match_format_table():
+    """Setting one of the 96 scale bits moves exactly the field the table names."""
+    table = _read_table("q4k_scale_layout.txt")
+    expect = {}
+    for byte, blo, bhi, field, sub, shift in table:
+        for b in range(int(blo), int(bhi) + 1):
+            expect[(int(byte), b)] = (field, int(sub), 1 << (b - int(blo) + int(shift)))
+    assert len(expect) == 96
+    for (byte, bit), (field, sub, val) in expect.items():
+        s = np.zeros(12, dtype=np.uint8)
+        s[byte] = 1 << bit
+        fields = {}
+        for j in range(8):
+            sc, m = oracle.scale_min(s, j)
+            fields[("sc", j)] = sc
+            fields[("m", j)] = m
+        nonzero = {k: v for k, v in fields.items() if v}
+        assert nonzero == {(field, sub): val}, (byte, bit, nonzero)
+
+
+def test_scale_pack_inverts_unpack_exhaustively_per_slot():
+    rng = np.random.Generator(np.random.PCG64(11))
+    for j in range(8):
+        for sc in range(64):
+            for m in range(64):
+                scs = rng.integers(0, 64, 8)
+                ms = rng.integers(0, 64, 8)
+                scs[j], ms[j] = sc, m
+                s = oracle.pack_scale_min(scs, ms)
+                for jj in range(8):
+                    assert oracle.scale_min(s, jj) == (scs[jj], ms[jj])
+
+
+def test_code_positions_match_format_table():
+    """A single code of 1 (d=1, every sc=63, dmin=0) lights exactly the weight the table names."""
+    table = _read_table("q4k_code_layout.txt")
+    where = {}
+    for first, last, nib, w0 in table:
+        for t in range(int(last) - int(first) + 1):
+            where[(int(first) + t, nib)] = int(w0) + t
+    assert sorted(where.values()) == list(range(256))
+    for (byte, nib), widx in where.items():
+        qs = np.zeros(128, dtype=np.uint8)
+        qs[byte] = 1 if nib == "low" else 16
+        vals = oracle.decode_block(_block(_h(1.0), 0, [0xFF] * 12, qs))
+        want = np.zeros(256)
+        want[widx] = 63.0
+        assert np.array_equal(vals, want), (byte, nib)
+
+
+# ------------------------------------------------------------ closed forms ----
+
+@pytest.mark.parametrize("d,dmin", [(1.0, 0.5), (2.0**-12, 2.0**-8), (0.0078125, 0.000244140625), (3.25, 0.0)])
+def test_closed_form_all_fields_max(d, dmin):
+    """All scale bits set gives sc_j = m_j = 63: q=15 -> 15*63*d - 63*dmin, q=0 -> -63*dmin."""
+    hi = oracle.decode_block(_block(_h(d), _h(dmin), [0xFF] * 12, [0xFF] * 128))
+    lo = oracle.decode_block(_block(_h(d), _h(dmin), [0xFF] * 12, [0x00] * 128))
+    assert np.all(hi == 15 * 63 * d - 63 * dmin)
+    assert np.all(lo == -63 * dmin)
+
+
+def test_closed_form_zero_codes_give_minus_dmin_m():
+    """sc_j = 0 and m_j = j+1 (bytes chosen by hand): every weight of sub-block j is -dmin*(j+1)."""
+    scales = [0, 0, 0, 0, 1, 2, 3, 4, 0x50, 0x60, 0x70, 0x80]
+    dmin = 0.0625
+    for qs in ([0] * 128, list(range(128))):
+        v = oracle.decode_block(_block(_h(0.5), _h(dmin), scales, qs))
+        for j in range(8):
+            assert np.all(v[32 * j:32 * j + 32] == -dmin * (j + 1))
+    # codes zero and arbitrary scales: still -dmin*m_j
+    scales2 = [0x3F, 0x15, 0x2A, 0x01, 1, 2, 3, 4, 0x5F, 0x6F, 0x7F, 0x8F]
+    v = oracle.decode_block(_block(_h(0.5), _h(dmin), scales2, [0] * 128))
+    for j in range(8):
+        assert np.all(v[32 * j:32 * j + 32] == -dmin * (j + 1))
+
+
+def test_closed_form_zero_d_dmin_gives_zero():
+    rng = np.random.Generator(np.random.PCG64(3))
+    blk = rng.integers(0, 256, 144, dtype=np.uint8)
+    blk[0:4] = 0
+    assert np.all(oracle.decode_block(blk) == 0.0)
+
+
+def test_closed_form_mixed_scales_and_codes():
+    """Hand-chosen fields: sc_j = 2j+1, m_j = 7-j; codes q = weight index % 16."""
+    # bytes derived by hand from the bit table for sc = (1,3,5,7,9,11,13,15), m = (7..0)
+    scales = [1, 3, 5, 7, 7, 6, 5, 4, 0x39, 0x2B, 0x1D, 0x0F]
+    qs = np.zeros(128, dtype=np.uint8)
+    for c in range(4):
+        for l in range(32):
+            lo_q = (64 * c + l) % 16
+            hi_q = (64 * c + 32 + l) % 16
+            qs[32 * c + l] = lo_q | (hi_q << 4)
+    d, dmin = 0.25, 0.125
+    v = oracle.decode_block(_block(_h(d), _h(dmin), scales, qs))
+    for i in range(256):
+        j = i // 32
+        assert v[i] == d * (2 * j + 1) * (i % 16) - dmin * (7 - j)
+
+
+def test_dequant_fp32_and_fp16_of_generated_weights():
+    """fp32 output = exact value (exact in fp32 for d, dmin in [2^-12, 2^-8]); fp16 = numpy's rounding of it."""
+    N, K = 16, 1024
+    w = synthetic.q4k_weights(N, K, seed=5)
+    exact = np.concatenate([oracle.decode_block(w[n, b * 144:(b + 1) * 144])
+                            for n in range(N) for b in range(K // 256)]).reshape(N, K)
+    f32 = oracle.dequant(w, N, K, "f32")
+    assert np.array_equal(f32.astype(np.float64), exact)
+    f16 = oracle.dequant(w, N, K, "f16")
+    assert np.array_equal(f16.view(np.uint16), f32.astype(np.float16).view(np.uint16))
+
+
+def test_dequant_fp32_rounds_once_for_wide_exponents():
+    """d large, dmin tiny: the difference needs more than 24 bits and is rounded once to fp32."""
+    blk = _block(_h(2048.0), _h(2.0**-24), [0xFF] * 12, [0x11] * 128)
+    v = oracle.decode_block(blk)
+    exact = 2048.0 * 63 * 1 - 2.0**-24 * 63
+    assert np.all(v == exact)
+    f32 = oracle.dequant(blk, 1, 256, "f32")
+    assert np.all(f32 == np.float32(exact))
+    assert float(np.float32(exact)) != exact
+
+
+# ------------------------------------------------------------- round trip ----
+
+def test_quantize_dequantize_round_trip_error():
+    rng = np.random.Generator(np.random.PCG64(21))
+    N, K = 8, 1024
+    w = rng.standard_normal((N, K))
+    q = oracle.quantize(w)
+    back = _exact_w(q, N, K)
+    err = back - w
+    var_expect = []
+    for n in range(N):
+        for b in range(K // 256):
+            blk = q[n, b * 144:(b + 1) * 144]
+            d, dmin = oracle.half_bits_to_double(blk[0:4].copy().view("<u2"))
+            for j in range(8):
+                sc, _ = oracle.scale_min(blk[4:16], j)
+                step = d * sc
+                e = err[n, b * 256 + 32 * j: b * 256 + 32 * j + 32]
+                assert np.all(np.abs(e) <= 0.5 * max(step, dmin) * (1 + 1e-9) + 1e-12)
+                var_expect.append(step * step / 12.0)
+    rms = math.sqrt(float(np.mean(err ** 2)))
+    rms_expect = math.sqrt(float(np.mean(var_expect)))
+    assert 0.75 * rms_expect <= rms <= 1.25 * rms_expect
+
+
+def test_exact_codes_round_trip():
+    """Blocks whose every sub-block uses q=0 and q=15, with max sc = max m = 63, come back exactly."""
+    rng = np.random.Generator(np.random.PCG64(33))
+    for trial in range(40):
+        sc = rng.integers(1, 64, 8)
+        m = rng.integers(0, 64, 8)
+        sc[rng.integers(0, 8)] = 63
+        m[rng.integers(0, 8)] = 63
+        codes = rng.integers(0, 16, 256)
+        for j in range(8):
+            pos = rng.choice(32, 2, replace=False) + 32 * j
+            codes[pos[0]], codes[pos[1]] = 0, 15
+        qs = np.zeros(128, dtype=np.uint8)
+        for i in range(256):
+            c, r = divmod(i, 64)
+            if r < 32:
+                qs[32 * c + r] |= codes[i]
+            else:
+                qs[32 * c + r - 32] |= codes[i] << 4
+        d = float(np.float16(rng.uniform(2**-12, 2**-8)))
+        dmin = float(np.float16(rng.uniform(2**-12, 2**-8)))
+        blk = _block(_h(d), _h(dmin), oracle.pack_scale_min(sc, m), qs)
+        v = oracle.decode_block(blk)
+        v2 = oracle.decode_block(oracle.quantize(v.reshape(1, 256)).reshape(144))
+        assert np.array_equal(v, v2), trial
+
+
+# ----------------------------------------------------------------- matmul ----
+
+def _exact_w(w, N, K):
+    return np.concatenate([oracle.decode_block(w[n, b * 144:(b + 1) * 144])
+                           for n in range(N) for b in range(K // 256)]).reshape(N, K)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 3, 256), (2, 5, 512), (5, 8, 256), (3, 1, 512)])
+def test_matmul_brute_force_tiny(M, N, K):
+    w = synthetic.q4k_weights(N, K, seed=100 + M * 10 + N)
+    x = synthetic.activations(M, K, seed=200 + M)
+    y, s = oracle.matmul(w, x, N, K)
+    W = _exact_w(w, N, K)
+    xd = x.astype(np.float64)
+    for m in range(M):
+        for n in range(N):
+            terms = [float(xd[m, k]) * float(W[n, k]) for k in range(K)]
+            ref = math.fsum(terms)
+            mag = math.fsum(abs(t) for t in terms)
+            assert abs(y[m, n] - ref) <= 1e-13 * mag + 1e-300
+            assert abs(s[m, n] - mag) <= 1e-13 * mag
+
+
+def test_matmul_unit_vectors_pick_columns():
+    N, K = 6, 512
+    w = synthetic.q4k_weights(N, K, seed=9)
+    W = _exact_w(w, N, K)
+    ks = [0, 1, 31, 32, 63, 64, 255, 256, 300, 511]
+    x = np.zeros((len(ks), K))
+    for i, k in enumerate(ks):
+        x[i, k] = 1.0
+    y, s = oracle.matmul(w, x, N, K)
+    for i, k in enumerate(ks):
+        assert np.array_equal(y[i], W[:, k])
+        assert np.array_equal(s[i], np.abs(W[:, k]))
+
+
+def test_matmul_ones_gives_row_sums_and_linearity():
+    N, K = 7, 768
+    w = synthetic.q4k_weights(N, K, seed=10)
+    W = _exact_w(w, N, K)
+    y, _ = oracle.matmul(w, np.ones((1, K)), N, K)
+    assert np.allclose(y[0], W.sum(axis=1), rtol=1e-14, atol=1e-14)
+    x1 = synthetic.activations(2, K, seed=1).astype(np.float64)
+    x2 = synthetic.activations(2, K, seed=2).astype(np.float64)
+    a, b = 0.75, -2.5
+    y1, s1 = oracle.matmul(w, x1, N, K)
+    y2, s2 = oracle.matmul(w, x2, N, K)
+    y3, _ = oracle.matmul(w, a * x1 + b * x2, N, K)
+    assert np.all(np.abs(y3 - (a * y1 + b * y2)) <= 1e-13 * (abs(a) * s1 + abs(b) * s2))
+
+
+def test_matmul_bound_and_cols_subset():
+    N, K, M = 9, 512, 3
+    w = synthetic.q4k_weights(N, K, seed=12)
+    x = synthetic.activations(M, K, seed=13, per_token_scale=True)
+    y, s = oracle.matmul(w, x, N, K)
+    W = _exact_w(w, N, K)
+    assert np.allclose(s, np.abs(x.astype(np.float64)) @ np.abs(W).T, rtol=1e-13)
+    assert np.allclose(y, x.astype(np.float64) @ W.T, rtol=1e-12, atol=1e-12)
+    cols = [8, 0, 4]
+    yc, sc = oracle.matmul_cols(w, x, N, K, cols)
+    assert np.array_equal(yc, y[:, cols])
+    assert np.array_equal(sc, s[:, cols])
+
+
+# ----------------------------------------------------------------- SwiGLU ----
+
+def test_swiglu_against_closed_forms():
+    scipy_special = pytest.importorskip("scipy.special")
+    g = np.array([0.0, 1.0, -1.0, 30.0, -30.0, 800.0, -800.0, 2.5])
+    u = np.array([3.0, 2.0, 2.0, 1.0, 1.0, 1.0, 1.0, -4.0])
+    h = oracle.swiglu(g, u)
+    assert h[0] == 0.0
+    assert h[3] == pytest.approx(30.0, rel=1e-12)
+    assert abs(h[4]) < 1e-11
+    assert h[5] == 800.0 and h[6] == 0.0
+    ref = g * scipy_special.expit(g) * u
+    assert np.allclose(h, ref, rtol=1e-14, atol=1e-300)
+    assert h[1] == pytest.approx(2.0 / (1.0 + math.exp(-1.0)), rel=1e-15)
+
+
+# ------------------------------------------------------- synthetic inputs ----
+
+def test_synthetic_weights_distribution():
+    w = synthetic.q4k_weights(64, 2560, seed=1)
+    assert w.shape == (64, 10 * 144)
+    blk = w.reshape(-1, 144)
+    d = blk[:, 0:2].copy().view("<f2").astype(np.float64).ravel()
+    dmin = blk[:, 2:4].copy().view("<f2").astype(np.float64).ravel()
+    for v in (d, dmin):
+        assert v.min() >= 2.0**-12 and v.max() <= 2.0**-8
+        assert v.max() > 0.9 * 2.0**-8 and v.min() < 1.1 * 2.0**-12
+    seen_sc, seen_m = set(), set()
+    for b in blk[:200]:
+        for j in range(8):
+            sc, m = oracle.scale_min(b[4:16], j)
+            seen_sc.add(sc)
+            seen_m.add(m)
+    assert seen_sc == set(range(64)) and seen_m == set(range(64))
+    assert np.array_equal(w, synthetic.q4k_weights(64, 2560, seed=1))
+    assert not np.array_equal(w, synthetic.q4k_weights(64, 2560, seed=2))
+
+
+def test_synthetic_activations():
+    x = synthetic.activations(4, 4096, seed=3)
+    assert x.dtype == np.float16 and x.shape == (4, 4096)
+    assert abs(float(x.astype(np.float64).mean())) < 0.05
+    assert abs(float(x.astype(np.float64).std()) - 1.0) < 0.05
+    xs = synthetic.activations(64, 1024, seed=4, per_token_scale=True).astype(np.float64)
+    sd = xs.std(axis=1)
+    assert sd.min() > 0.4 and sd.max() < 2.3
