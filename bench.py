@@ -1,0 +1,395 @@
+"""Benchmark of the Q4_K dequant-fused matmul on one or more GPUs.
+
+Headline: the decode sweep -- M = 1 GEMV over the seven Qwen3-4B layer shapes
+(q, k, v, o, gate, up, down) of all 36 layers, 2.04 GB of distinct seeded Q4_K
+weights resident in HBM (larger than L2, so every call streams from HBM), one
+CUDA-graph replay per step.  value = weight bytes streamed / time (GB/s).
+Second object: the long-prompt prefill sweep at M = 2048 over the same
+weights (tcgen05 path), TFLOP/s = 2*M*N*K / time.
+
+Multi-GPU: replicas only.  Each rank runs the same sweep on its own GPU with
+no collective on the data path; value = bytes all ranks streamed / max time.
+
+--impl reference times the CPU oracle (single thread, fp64) on a bounded
+sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synthetic  # noqa: E402
+
+SHAPES = synthetic.LAYER_SHAPES
+N_LAYERS = synthetic.N_LAYERS
+M_PREFILL = 2048
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--layers", type=int, default=N_LAYERS)
+    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--per-shape", action="store_true", help="also time each shape alone (stderr)")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def weight_bytes(N, K):
+    return N * (K // 256) * 144
+
+
+# ------------------------------------------------------------ clock sampler --
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.rows = []
+        self._stop = threading.Event()
+        self._t = None
+
+    def _run(self):
+        while not self._stop.is_set():
+            try:
+                out = subprocess.run(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                                      "--format=csv,noheader,nounits"], capture_output=True, text=True, timeout=5)
+                if out.returncode == 0 and out.stdout.strip():
+                    self.rows.append([c.strip() for c in out.stdout.strip().split(",")])
+            except Exception:
+                pass
+            self._stop.wait(0.2)
+
+    def __enter__(self):
+        self._t = threading.Thread(target=self._run, daemon=True)
+        self._t.start()
+        return self
+
+    def __exit__(self, *a):
+        self._stop.set()
+        self._t.join(timeout=10)
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4) if len(r) > 5 + i and r[5 + i] == "Active"})
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows)}
+
+
+# ---------------------------------------------------------------- our arm --
+def build_inputs(torch, dev, layers):
+    """Seeded weights (host numpy -> device) and activations for the sweep."""
+    W, X, Y, meta = [], [], [], []
+    for layer in range(layers):
+        for idx, (name, K, N) in enumerate(SHAPES):
+            w = synthetic.q4k_weights(N, K, synthetic.weight_seed(1, layer, idx))
+            W.append(torch.from_numpy(w).to(dev))
+            X.append(torch.from_numpy(synthetic.activations(1, K, synthetic.activation_seed(1, layer * 8 + idx))
+                                      .reshape(K)).to(dev))
+            Y.append(torch.empty(N, dtype=torch.float32, device=dev))
+            meta.append((name, K, N))
+    return W, X, Y, meta
+
+
+def time_graph(torch, graph, stream, steps, warmup):
+    for _ in range(warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        graph.replay()
+    end.record(stream)
+    end.synchronize()
+    return start.elapsed_time(end) / 1e3 / steps  # seconds per step
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import bit_q4_weight_gb300 as q
+
+    layers = args.layers
+    W, X, Y, meta = build_inputs(torch, dev, layers)
+    total_bytes = sum(weight_bytes(N, K) for (_, K, N) in meta)
+    n_launch = len(meta)
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+
+    def sweep():
+        for w, x, y, (_, K, N) in zip(W, X, Y, meta):
+            q.jllm_q4k_gemv(w, x, N, K, out=y)
+
+    with torch.cuda.stream(stream):
+        sweep()  # eager warm-up (first launches set kernel attributes)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        sweep()
+    torch.cuda.synchronize()
+
+    if world > 1:
+        dist.barrier()
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize()
+        t_step = time_graph(torch, g, stream, args.steps, args.warmup)
+    clocks = clk.summary()
+    t_max = t_step
+    if world > 1:
+        tt = torch.tensor([t_step], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_max = float(tt.item())
+    value = total_bytes * world / t_max / 1e9
+
+    # end to end: host->device copy of every activation, the sweep, device->host of every output
+    xs_host = torch.cat([x.cpu() for x in X]).pin_memory()
+    ys_host = torch.empty(sum(y.numel() for y in Y), dtype=torch.float32).pin_memory()
+    x_dev_all = torch.empty_like(xs_host, device=dev)
+    y_dev_all = torch.empty(ys_host.numel(), dtype=torch.float32, device=dev)
+    offs_x = np.cumsum([0] + [x.numel() for x in X])
+    offs_y = np.cumsum([0] + [y.numel() for y in Y])
+    Xv = [x_dev_all[offs_x[i]:offs_x[i + 1]] for i in range(n_launch)]
+    Yv = [y_dev_all[offs_y[i]:offs_y[i + 1]] for i in range(n_launch)]
+    ge = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        for w, x, y, (_, K, N) in zip(W, Xv, Yv, meta):
+            q.jllm_q4k_gemv(w, x, N, K, out=y)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(ge, stream=stream):
+        for w, x, y, (_, K, N) in zip(W, Xv, Yv, meta):
+            q.jllm_q4k_gemv(w, x, N, K, out=y)
+    torch.cuda.synchronize()
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            x_dev_all.copy_(xs_host, non_blocking=True)
+            ge.replay()
+            ys_host.copy_(y_dev_all, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(args.warmup):
+        e2e_step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        e2e_step()
+    t_e2e = (time.perf_counter() - t0) / args.steps
+    if world > 1:
+        tt = torch.tensor([t_e2e], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_e2e = float(tt.item())
+    e2e = {"value": round(total_bytes * world / t_e2e / 1e9, 2), "unit": "GB/s",
+           "h2d_bytes_per_step": int(xs_host.numel() * 2), "d2h_bytes_per_step": int(ys_host.numel() * 4)}
+
+    peaks = {}
+    pk_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(pk_path):
+        peaks = json.load(open(pk_path))
+    hbm_peak = peaks.get("hbm_gbs", 6800.0)
+    peak_note = "measured" if "hbm_gbs" in peaks else "fallback"
+
+    per_shape = {}
+    if args.per_shape and rank == 0:
+        for idx, (name, K, N) in enumerate(SHAPES):
+            sel = [i for i in range(n_launch) if i % len(SHAPES) == idx]
+            gs = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gs, stream=stream):
+                for i in sel:
+                    q.jllm_q4k_gemv(W[i], X[i], N, K, out=Y[i])
+            torch.cuda.synchronize()
+            t = time_graph(torch, gs, stream, max(3, args.steps // 2), 2)
+            per_shape[name] = round(len(sel) * weight_bytes(N, K) / t / 1e9, 1)
+            del gs
+
+    prefill = None
+    if not args.no_prefill:
+        prefill = run_prefill(torch, q, W, meta, dev, stream, args, world)
+
+    if rank == 0:
+        line = {
+            "metric": "Q4_K matmul: M=1 weight GB/s vs HBM peak; M=2048 TFLOP/s vs BF16 peak",
+            "value": round(value, 2),
+            "unit": "GB/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(t_max * 1e3, 4),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "q4k-f16-f32",
+            "data": "synthetic (seeded GGUF Q4_K blocks, fp16 N(0,1) activations)",
+            "config": {"workload": f"decode sweep M=1, {layers} layers x 7 Qwen3-4B shapes",
+                       "weight_bytes_per_step": total_bytes, "launches_per_step": n_launch,
+                       "l2": "inputs larger than L2 (2.04 GB of weights cycled)", "parallelism": f"replicas{world}"},
+            "gpu_launches": n_launch * args.steps,
+            "clocks": clocks,
+            "roofline": {"bound": "hbm", "achieved": round(total_bytes / t_step / 1e9, 2), "peak": hbm_peak,
+                         "unit": "GB/s", "frac": round(total_bytes / t_step / 1e9 / hbm_peak, 4),
+                         "traffic": None, "peak_source": peak_note,
+                         "kernel": "q4k_gemv_kernel", "avg_launch_us": round(t_step / n_launch * 1e6, 3)},
+            "e2e": e2e,
+        }
+        if per_shape:
+            line["per_shape_gbs"] = per_shape
+        if prefill:
+            line["prefill_m2048"] = prefill
+        if not args.no_cpu_baseline and world == 1:
+            line["cpu_baseline"] = cpu_baseline(budget_s=12.0)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def run_prefill(torch, q, W, meta, dev, stream, args, world):
+    """M = 2048 tcgen05 GEMMs over the same resident weights, fp16 out."""
+    M = M_PREFILL
+    xs = {}
+    for (_, K, N) in meta:
+        if K not in xs:
+            xs[K] = torch.from_numpy(synthetic.activations(M, K, synthetic.activation_seed(3, M, K))).to(dev)
+    ys = {N: torch.empty((M, N), dtype=torch.float16, device=dev) for (_, K, N) in meta}
+    flops = sum(2.0 * M * N * K for (_, K, N) in meta)
+
+    def sweep():
+        for w, (_, K, N) in zip(W, meta):
+            q.jllm_q4k_gemm(w, xs[K], N, K, out=ys[N])
+
+    with torch.cuda.stream(stream):
+        sweep()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        sweep()
+    torch.cuda.synchronize()
+    steps = max(2, args.steps // 5)
+    with ClockSampler(int(os.environ.get("LOCAL_RANK", "0"))) as clk:
+        t = time_graph(torch, g, stream, steps, max(1, args.warmup // 2))
+    peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
+        os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
+    peak = peaks.get("bf16_tflops_sustained", 1700.0)
+    tf = flops / t / 1e12
+    del g
+    return {"value": round(tf * world, 2), "unit": "TFLOP/s", "ms_per_step": round(t * 1e3, 3),
+            "config": {"workload": f"prefill sweep M={M}, {len(meta) // 7} layers x 7 shapes, fp16 out",
+                       "flops_per_step": flops, "launches_per_step": len(meta)},
+            "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": peak, "unit": "TFLOP/s",
+                         "frac": round(tf / peak, 4), "traffic": None,
+                         "peak_source": "measured bf16 sustained (fp16 dense rate equal)",
+                         "kernel": "q4k_gemm_tc_kernel"},
+            "clocks": clk.summary()}
+
+
+# ------------------------------------------------------------ CPU baseline --
+def cpu_baseline(budget_s=12.0):
+    """The oracle (single-threaded fp64 C) on the first layers of the decode sweep, bounded in time."""
+    import oracle
+
+    oracle.build()
+    done_bytes = 0
+    t_total = 0.0
+    layers = 0
+    for layer in range(N_LAYERS):
+        for idx, (name, K, N) in enumerate(SHAPES):
+            w = synthetic.q4k_weights(N, K, synthetic.weight_seed(1, layer, idx))
+            x = synthetic.activations(1, K, synthetic.activation_seed(1, layer * 8 + idx))
+            t0 = time.perf_counter()
+            oracle.matmul(w, x, N, K)
+            t_total += time.perf_counter() - t0
+            done_bytes += weight_bytes(N, K)
+        layers += 1
+        if t_total >= budget_s:
+            break
+    return {"value": round(done_bytes / t_total / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"decode sweep, first {layers} of 36 layers x 7 shapes ({done_bytes} weight bytes), "
+                      f"{t_total:.1f} s single-threaded fp64"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+
+    oracle.build()
+    # each step: one layer of the decode sweep (7 shapes), cycling layers
+    per_step_bytes = sum(weight_bytes(N, K) for (_, K, N) in SHAPES)
+    inputs = []
+    n_layers = min(N_LAYERS, args.warmup + args.steps)
+    for layer in range(n_layers):
+        inputs.append([(synthetic.q4k_weights(N, K, synthetic.weight_seed(1, layer, idx)),
+                        synthetic.activations(1, K, synthetic.activation_seed(1, layer * 8 + idx)), N, K)
+                       for idx, (_, K, N) in enumerate(SHAPES)])
+
+    def step(i):
+        for w, x, N, K in inputs[i % n_layers]:
+            oracle.matmul(w, x, N, K)
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    t = (time.perf_counter() - t0) / args.steps
+    v = per_step_bytes / t / 1e9
+    line = {
+        "impl": "reference",
+        "metric": "Q4_K matmul: M=1 weight GB/s vs HBM peak; M=2048 TFLOP/s vs BF16 peak",
+        "value": round(v, 4), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(t * 1e3, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic (seeded GGUF Q4_K blocks, fp16 N(0,1) activations)",
+        "config": {"workload": "decode sweep M=1, one layer (7 Qwen3-4B shapes) per step, single-threaded CPU oracle"},
+        "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{args.steps} layers of the decode sweep, one per step"},
+        "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

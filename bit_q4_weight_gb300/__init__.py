@@ -1,0 +1,229 @@
+"""Python binding of libjllm_q4k.so, the GB300 (sm_103a) Q4_K dequant-fused matmul library.
+
+Argument marshalling only: every function checks tensor dtypes, shapes,
+devices and contiguity, allocates the output tensor when none is given, and
+calls the C entry point of the same name (include/jllm_q4k.h) on the current
+torch CUDA stream.  All computation happens in the library's CUDA kernels;
+there is no CPU fallback, and importing this module fails loudly when the
+library has not been built.
+
+Layouts (see the header): W is uint8 [N, K/256*144] (GGUF Q4_K super-blocks,
+rows contiguous), X is fp16 [M, K], Y is [M, N] fp32 or fp16.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import _build
+
+LIB_PATH = _build.LIB
+BLOCK_BYTES = 144
+QK = 256
+
+# status codes (jllm_status)
+JLLM_OK = 0
+JLLM_ERR_INVALID_ARG = 1
+JLLM_ERR_UNSUPPORTED_SHAPE = 2
+JLLM_ERR_MISALIGNED = 3
+JLLM_ERR_UNSUPPORTED_DTYPE = 4
+JLLM_ERR_WORKSPACE = 5
+JLLM_ERR_CUDA = 6
+JLLM_ERR_DEVICE_TIMEOUT = 7
+JLLM_ERR_NO_DEVICE = 8
+# dtypes (jllm_dtype)
+JLLM_F32 = 0
+JLLM_F16 = 1
+
+# Every symbol include/jllm_q4k.h declares.
+EXPORTS = (
+    "jllm_q4k_dequant",
+    "jllm_q4k_gemv",
+    "jllm_q4k_gemm",
+    "jllm_q4k_ffn_swiglu",
+    "jllm_q4k_workspace_bytes",
+    "jllm_q4k_gemv_max_m",
+    "jllm_get_device_error",
+    "jllm_status_string",
+)
+
+
+class JllmError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {status_string(status)} ({status})")
+        self.status = status
+
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build it first (python -c 'import __graft_entry__ as g; g.build()' "
+        "or python bit_q4_weight_gb300/_build.py)"
+    )
+
+lib = ctypes.CDLL(LIB_PATH)
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_SZ = ctypes.c_size_t
+_ST = ctypes.c_int
+
+lib.jllm_q4k_dequant.argtypes = [_P, _P, ctypes.c_int, _I64, _I64, _P]
+lib.jllm_q4k_dequant.restype = _ST
+lib.jllm_q4k_gemv.argtypes = [_P, _P, _P, _I64, _I64, _P, _SZ, _P]
+lib.jllm_q4k_gemv.restype = _ST
+lib.jllm_q4k_gemm.argtypes = [_P, _P, _P, ctypes.c_int, _I64, _I64, _I64, _P, _SZ, _P]
+lib.jllm_q4k_gemm.restype = _ST
+lib.jllm_q4k_ffn_swiglu.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P]
+lib.jllm_q4k_ffn_swiglu.restype = _ST
+lib.jllm_q4k_workspace_bytes.argtypes = [_I64, _I64, _I64]
+lib.jllm_q4k_workspace_bytes.restype = _SZ
+lib.jllm_q4k_gemv_max_m.argtypes = []
+lib.jllm_q4k_gemv_max_m.restype = ctypes.c_int
+lib.jllm_get_device_error.argtypes = [_P]
+lib.jllm_get_device_error.restype = _ST
+lib.jllm_status_string.argtypes = [_ST]
+lib.jllm_status_string.restype = ctypes.c_char_p
+
+
+def status_string(status: int) -> str:
+    return lib.jllm_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str) -> None:
+    if status != JLLM_OK:
+        raise JllmError(status, where)
+
+
+# ------------------------------------------------------------ tensor helpers --
+
+def _torch():
+    import torch
+
+    return torch
+
+
+def _stream_ptr(stream) -> int:
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def _need(t, dtype, shape, name):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def _w_shape(N: int, K: int):
+    return (N, K // QK * BLOCK_BYTES)
+
+
+def _ws(M, N, K, ws, device):
+    need = int(lib.jllm_q4k_workspace_bytes(M, N, K))
+    if need == 0:
+        return None, 0
+    torch = _torch()
+    if ws is None:
+        ws = torch.empty(need, dtype=torch.uint8, device=device)
+    return ws, ws.numel() * ws.element_size()
+
+
+# ------------------------------------------------------------------ the API --
+
+def jllm_q4k_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(lib.jllm_q4k_workspace_bytes(M, N, K))
+
+
+def jllm_q4k_gemv_max_m() -> int:
+    return int(lib.jllm_q4k_gemv_max_m())
+
+
+def jllm_get_device_error(stream=None) -> int:
+    """Synchronise the stream and return the device error status (0 = JLLM_OK)."""
+    return int(lib.jllm_get_device_error(_stream_ptr(stream)))
+
+
+def jllm_q4k_dequant(w, N: int, K: int, out_dtype=None, out=None, stream=None):
+    """dequant(W) as an [N, K] fp32 (default) or fp16 tensor."""
+    torch = _torch()
+    out_dtype = out_dtype or (out.dtype if out is not None else torch.float32)
+    if out_dtype not in (torch.float32, torch.float16):
+        raise TypeError("out_dtype must be torch.float32 or torch.float16")
+    _need(w, torch.uint8, _w_shape(N, K), "w")
+    if out is None:
+        out = torch.empty((N, K), dtype=out_dtype, device=w.device)
+    _need(out, out_dtype, (N, K), "out")
+    dt = JLLM_F16 if out_dtype == torch.float16 else JLLM_F32
+    _check(lib.jllm_q4k_dequant(w.data_ptr(), out.data_ptr(), dt, N, K, _stream_ptr(stream)), "jllm_q4k_dequant")
+    return out
+
+
+def jllm_q4k_gemv(w, x, N: int, K: int, out=None, ws=None, stream=None):
+    """y[N] (fp32) = dequant(W) x for one fp16 activation row x[K]."""
+    torch = _torch()
+    _need(w, torch.uint8, _w_shape(N, K), "w")
+    if x.dim() == 2 and x.shape[0] == 1:
+        x = x.view(K)
+    _need(x, torch.float16, (K,), "x")
+    if out is None:
+        out = torch.empty((N,), dtype=torch.float32, device=w.device)
+    _need(out, torch.float32, (N,), "out")
+    ws, nbytes = _ws(1, N, K, ws, w.device)
+    _check(
+        lib.jllm_q4k_gemv(w.data_ptr(), x.data_ptr(), out.data_ptr(), N, K,
+                          ws.data_ptr() if ws is not None else None, nbytes, _stream_ptr(stream)),
+        "jllm_q4k_gemv",
+    )
+    return out
+
+
+def jllm_q4k_gemm(w, x, N: int, K: int, out_dtype=None, out=None, ws=None, stream=None):
+    """Y[M, N] = X[M, K] dequant(W)^T; fp32 (default) or fp16 output."""
+    torch = _torch()
+    _need(w, torch.uint8, _w_shape(N, K), "w")
+    if x.dim() != 2:
+        raise ValueError("x must be [M, K]")
+    M = int(x.shape[0])
+    _need(x, torch.float16, (M, K), "x")
+    out_dtype = out_dtype or (out.dtype if out is not None else torch.float32)
+    if out_dtype not in (torch.float32, torch.float16):
+        raise TypeError("out_dtype must be torch.float32 or torch.float16")
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=w.device)
+    _need(out, out_dtype, (M, N), "out")
+    ws, nbytes = _ws(M, N, K, ws, w.device)
+    dt = JLLM_F16 if out_dtype == torch.float16 else JLLM_F32
+    _check(
+        lib.jllm_q4k_gemm(w.data_ptr(), x.data_ptr(), out.data_ptr(), dt, M, N, K,
+                          ws.data_ptr() if ws is not None else None, nbytes, _stream_ptr(stream)),
+        "jllm_q4k_gemm",
+    )
+    return out
+
+
+def jllm_q4k_ffn_swiglu(w_gate, w_up, x, N: int, K: int, out=None, ws=None, stream=None):
+    """h[M, N] (fp16) = silu(X Wg^T) * (X Wu^T)."""
+    torch = _torch()
+    _need(w_gate, torch.uint8, _w_shape(N, K), "w_gate")
+    _need(w_up, torch.uint8, _w_shape(N, K), "w_up")
+    if x.dim() != 2:
+        raise ValueError("x must be [M, K]")
+    M = int(x.shape[0])
+    _need(x, torch.float16, (M, K), "x")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    _need(out, torch.float16, (M, N), "out")
+    ws, nbytes = _ws(M, N, K, ws, x.device)
+    _check(
+        lib.jllm_q4k_ffn_swiglu(w_gate.data_ptr(), w_up.data_ptr(), x.data_ptr(), out.data_ptr(), M, N, K,
+                                ws.data_ptr() if ws is not None else None, nbytes, _stream_ptr(stream)),
+        "jllm_q4k_ffn_swiglu",
+    )
+    return out

@@ -1,0 +1,176 @@
+// C ABI of the Q4_K library (include/jllm_q4k.h): argument checks, the
+// M-threshold dispatch between the GEMV and the tcgen05 GEMM, and status
+// mapping.  Nothing here allocates device memory.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stdlib.h>
+
+#include <mutex>
+
+#include "../../include/jllm_q4k.h"
+#include "internal.h"
+
+namespace jllm {
+
+namespace {
+constexpr int kMaxDevices = 64;
+DevInfo g_dev[kMaxDevices];
+std::once_flag g_dev_once[kMaxDevices];
+}  // namespace
+
+const DevInfo& device_info() {
+  static thread_local DevInfo bad;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    bad.err = e != cudaSuccess ? e : cudaErrorInvalidDevice;
+    return bad;
+  }
+  std::call_once(g_dev_once[dev], [dev]() {
+    DevInfo& d = g_dev[dev];
+    d.device = dev;
+    cudaError_t err = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
+    if (err == cudaSuccess) err = cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (err == cudaSuccess) err = cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev);
+    int optin = 0;
+    if (err == cudaSuccess) err = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    d.smem_optin = (size_t)optin;
+    const char* env = getenv("JLLM_PDL");
+    d.pdl = !(env && env[0] == '0');
+    d.err = err;
+  });
+  return g_dev[dev];
+}
+
+}  // namespace jllm
+
+namespace {
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+// The kernels index rows and blocks with 32-bit integers.
+constexpr int64_t kMaxRows = (int64_t)1 << 30;
+constexpr int64_t kMaxK = (int64_t)1 << 24;
+
+jllm_status check_shape(int64_t M, int64_t N, int64_t K) {
+  if (M < 1 || N < 1) return JLLM_ERR_INVALID_ARG;
+  if (K < 256 || K % 256 != 0) return JLLM_ERR_UNSUPPORTED_SHAPE;
+  if (M > kMaxRows || N > kMaxRows || K > kMaxK) return JLLM_ERR_UNSUPPORTED_SHAPE;
+  return JLLM_OK;
+}
+
+jllm_status check_workspace(void* ws, size_t ws_bytes, size_t need) {
+  if (need == 0) return JLLM_OK;
+  if (ws == nullptr || ws_bytes < need || !aligned16(ws)) return JLLM_ERR_WORKSPACE;
+  return JLLM_OK;
+}
+
+jllm_status check_device() {
+  const jllm::DevInfo& d = jllm::device_info();
+  if (d.err != cudaSuccess) return JLLM_ERR_CUDA;
+  if (d.major != 10 || d.minor != 3) return JLLM_ERR_NO_DEVICE;
+  return JLLM_OK;
+}
+
+jllm_status from_cuda(cudaError_t e) { return e == cudaSuccess ? JLLM_OK : JLLM_ERR_CUDA; }
+
+int g_gemv_max_m = 1;
+std::once_flag g_thresh_once;
+
+int gemv_max_m() {
+  std::call_once(g_thresh_once, []() {
+    const char* env = getenv("JLLM_GEMV_MAX_M");
+    if (env) {
+      const long v = strtol(env, nullptr, 10);
+      if (v >= 0 && v <= 1) g_gemv_max_m = (int)v;
+    }
+  });
+  return g_gemv_max_m;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* jllm_status_string(jllm_status status) {
+  switch (status) {
+    case JLLM_OK: return "JLLM_OK";
+    case JLLM_ERR_INVALID_ARG: return "JLLM_ERR_INVALID_ARG";
+    case JLLM_ERR_UNSUPPORTED_SHAPE: return "JLLM_ERR_UNSUPPORTED_SHAPE";
+    case JLLM_ERR_MISALIGNED: return "JLLM_ERR_MISALIGNED";
+    case JLLM_ERR_UNSUPPORTED_DTYPE: return "JLLM_ERR_UNSUPPORTED_DTYPE";
+    case JLLM_ERR_WORKSPACE: return "JLLM_ERR_WORKSPACE";
+    case JLLM_ERR_CUDA: return "JLLM_ERR_CUDA";
+    case JLLM_ERR_DEVICE_TIMEOUT: return "JLLM_ERR_DEVICE_TIMEOUT";
+    case JLLM_ERR_NO_DEVICE: return "JLLM_ERR_NO_DEVICE";
+  }
+  return "JLLM_ERR_UNKNOWN";
+}
+
+int jllm_q4k_gemv_max_m(void) { return gemv_max_m(); }
+
+size_t jllm_q4k_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  (void)M;
+  (void)N;
+  (void)K;
+  return 0;
+}
+
+jllm_status jllm_q4k_dequant(const void* w_q4k, void* out, jllm_dtype out_dt, int64_t N, int64_t K,
+                             jllm_stream_t stream) {
+  if (!w_q4k || !out) return JLLM_ERR_INVALID_ARG;
+  jllm_status st = check_shape(1, N, K);
+  if (st != JLLM_OK) return st;
+  if (out_dt != JLLM_F32 && out_dt != JLLM_F16) return JLLM_ERR_UNSUPPORTED_DTYPE;
+  if (!aligned16(w_q4k) || !aligned16(out)) return JLLM_ERR_MISALIGNED;
+  if ((st = check_device()) != JLLM_OK) return st;
+  return from_cuda(jllm::launch_dequant(w_q4k, out, out_dt == JLLM_F16, N, K, (cudaStream_t)stream));
+}
+
+jllm_status jllm_q4k_gemv(const void* w_q4k, const void* x, float* y, int64_t N, int64_t K, void* ws,
+                          size_t ws_bytes, jllm_stream_t stream) {
+  if (!w_q4k || !x || !y) return JLLM_ERR_INVALID_ARG;
+  jllm_status st = check_shape(1, N, K);
+  if (st != JLLM_OK) return st;
+  if (!aligned16(w_q4k) || !aligned16(x) || !aligned16(y)) return JLLM_ERR_MISALIGNED;
+  if ((st = check_workspace(ws, ws_bytes, jllm_q4k_workspace_bytes(1, N, K))) != JLLM_OK) return st;
+  if ((st = check_device()) != JLLM_OK) return st;
+  return from_cuda(jllm::launch_gemv(w_q4k, nullptr, x, y, N, K, (cudaStream_t)stream));
+}
+
+jllm_status jllm_q4k_gemm(const void* w_q4k, const void* x, void* y, jllm_dtype y_dt, int64_t M, int64_t N,
+                          int64_t K, void* ws, size_t ws_bytes, jllm_stream_t stream) {
+  if (!w_q4k || !x || !y) return JLLM_ERR_INVALID_ARG;
+  jllm_status st = check_shape(M, N, K);
+  if (st != JLLM_OK) return st;
+  if (y_dt != JLLM_F32 && y_dt != JLLM_F16) return JLLM_ERR_UNSUPPORTED_DTYPE;
+  if (!aligned16(w_q4k) || !aligned16(x) || !aligned16(y)) return JLLM_ERR_MISALIGNED;
+  if ((st = check_workspace(ws, ws_bytes, jllm_q4k_workspace_bytes(M, N, K))) != JLLM_OK) return st;
+  if ((st = check_device()) != JLLM_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (M <= gemv_max_m() && y_dt == JLLM_F32)
+    return from_cuda(jllm::launch_gemv(w_q4k, nullptr, x, y, N, K, s));
+  return from_cuda(jllm::launch_gemm_tc(w_q4k, nullptr, x, y, y_dt == JLLM_F16, M, N, K, s));
+}
+
+jllm_status jllm_q4k_ffn_swiglu(const void* w_gate, const void* w_up, const void* x, void* h, int64_t M,
+                                int64_t N, int64_t K, void* ws, size_t ws_bytes, jllm_stream_t stream) {
+  if (!w_gate || !w_up || !x || !h) return JLLM_ERR_INVALID_ARG;
+  jllm_status st = check_shape(M, N, K);
+  if (st != JLLM_OK) return st;
+  if (!aligned16(w_gate) || !aligned16(w_up) || !aligned16(x) || !aligned16(h)) return JLLM_ERR_MISALIGNED;
+  if ((st = check_workspace(ws, ws_bytes, jllm_q4k_workspace_bytes(M, N, K))) != JLLM_OK) return st;
+  if ((st = check_device()) != JLLM_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (M <= gemv_max_m()) return from_cuda(jllm::launch_gemv(w_gate, w_up, x, h, N, K, s));
+  return from_cuda(jllm::launch_gemm_tc(w_gate, w_up, x, h, true, M, N, K, s));
+}
+
+jllm_status jllm_get_device_error(jllm_stream_t stream) {
+  uint32_t bits = 0;
+  cudaError_t e = jllm::read_clear_gemm_error(&bits, (cudaStream_t)stream);
+  if (e != cudaSuccess) return JLLM_ERR_CUDA;
+  return bits ? JLLM_ERR_DEVICE_TIMEOUT : JLLM_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,39 @@
+// Internal launchers shared by the C ABI (api.cu) and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace jllm {
+
+struct DevInfo {
+  int device = -1;
+  int sm_count = 0;
+  int major = 0, minor = 0;
+  size_t smem_optin = 0;  // max dynamic shared memory per block
+  bool pdl = true;        // launch GEMV kernels with programmatic dependent launch
+  cudaError_t err = cudaSuccess;
+};
+
+// Properties of the current device (cached per device).
+const DevInfo& device_info();
+
+// out[N,K] = dequant(W); f16 selects fp16 output.
+cudaError_t launch_dequant(const void* w, void* out, bool f16, int64_t N, int64_t K, cudaStream_t s);
+
+// M = 1 GEMV.  w1 == nullptr: y = fp32 [N] = W0 x.  w1 != nullptr: y = fp16 [N]
+// = silu(W0 x) * (W1 x).
+cudaError_t launch_gemv(const void* w0, const void* w1, const void* x, void* y, int64_t N, int64_t K,
+                        cudaStream_t s);
+
+// TMA + tcgen05 GEMM for any M >= 1.  w1 != nullptr selects the SwiGLU
+// epilogue (y = fp16 h).  Returns cudaErrorInvalidValue for unsupported
+// shapes.
+cudaError_t launch_gemm_tc(const void* w0, const void* w1, const void* x, void* y, bool y_f16, int64_t M,
+                           int64_t N, int64_t K, cudaStream_t s);
+
+// Read and clear the device error word of the tcgen05 kernels.
+cudaError_t read_clear_gemm_error(uint32_t* bits, cudaStream_t s);
+
+}  // namespace jllm

@@ -1,0 +1,154 @@
+/*
+ * jllm_q4k.h -- C ABI of the GB300 (sm_103a) Q4_K dequant-fused matmul library.
+ *
+ * The library computes Y[M,N] = X[M,K] * dequant(W)[N,K]^T where W is a weight
+ * matrix stored as GGUF Q4_K super-blocks and X is fp16.  This is the work of
+ * the two kernels the genie-ai-runtime README lists under "At a glance"
+ * (Kernels bullet) and "Project layout" (src/kernels/): the "INT4
+ * dequant-fused GEMV" used for decode (M = 1) and the "tensor-core MMQ Q4_K
+ * prefill" used for prompts (M = prompt tokens); and of the SwiGLU part of its
+ * "fused RMSNorm + RoPE + SwiGLU" kernel.  The pages say the runtime loads
+ * GGUF Q4_K_M models ("At a glance", Models bullet) but print neither the
+ * block layout nor any kernel interface; both are defined here.
+ *
+ * ---------------------------------------------------------------- layouts --
+ * Q4_K super-block (144 bytes, 256 weights), public GGUF layout:
+ *   bytes 0..1    d     fp16 little endian        (scale of the 6-bit scales)
+ *   bytes 2..3    dmin  fp16 little endian        (scale of the 6-bit mins)
+ *   bytes 4..15   s[12] eight 6-bit scales sc_j and eight 6-bit mins m_j:
+ *                   j<4 : sc_j = s[j] & 63,  m_j = s[j+4] & 63
+ *                   j>=4: sc_j = (s[j+4] & 15) | (s[j-4] >> 6) << 4
+ *                         m_j  = (s[j+4] >> 4) | (s[j]   >> 6) << 4
+ *   bytes 16..143 qs[128] 4-bit codes q: weight 64c+l (c = 0..3, l = 0..31) is
+ *                 the low nibble of qs[32c+l], weight 64c+32+l its high nibble.
+ *   value of weight i (sub-block j = i/32): w = d*sc_j*q - dmin*m_j.
+ * W   : [N rows][K/256 blocks] of 144-byte blocks, rows contiguous (row pitch
+ *       K/256*144 bytes), device memory, 16-byte aligned.
+ * X   : [M][K] fp16 row-major, contiguous, device memory, 16-byte aligned.
+ * Y   : [M][N] row-major, contiguous, fp32 or fp16, device memory,
+ *       16-byte aligned.
+ * K must be a positive multiple of 256; M, N >= 1.  Sizes are element counts.
+ *
+ * ---------------------------------------------------------------- numerics --
+ * Dequant: fp32 output is d*sc*q - dmin*m evaluated in fp32 in that order
+ * (the three products are exact, the difference rounds once); fp16 output is
+ * that fp32 value rounded to nearest even.  Matmul outputs satisfy, per
+ * element, |y - y_ref| <= 2e-3 * sum_k |x_k * w_nk| + 1e-5 against the exact
+ * product of the fp16 X and the exact dequantised W.
+ *
+ * --------------------------------------------------------------- semantics --
+ * Every pointer argument is caller-owned device memory unless stated; the
+ * library never allocates or frees device memory on these calls.  `stream` is
+ * a cudaStream_t (NULL = legacy default stream).  Argument errors are
+ * reported synchronously, before anything is launched; otherwise the work is
+ * enqueued on `stream` and the call returns JLLM_OK without synchronising.
+ * A launch failure returns JLLM_ERR_CUDA.  Kernel-side waits are bounded: a
+ * wait that runs out sets a device error word that jllm_get_device_error()
+ * reads.  No call throws, prints or keeps state beyond cached device
+ * properties and a per-device table of driver entry points.
+ */
+#ifndef JLLM_Q4K_H
+#define JLLM_Q4K_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  JLLM_OK = 0,
+  JLLM_ERR_INVALID_ARG = 1,       /* NULL pointer, M/N < 1, bad enum value      */
+  JLLM_ERR_UNSUPPORTED_SHAPE = 2, /* K not a positive multiple of 256, or a
+                                     size beyond the kernels' index range      */
+  JLLM_ERR_MISALIGNED = 3,        /* a pointer not 16-byte aligned             */
+  JLLM_ERR_UNSUPPORTED_DTYPE = 4, /* output dtype not allowed for this call    */
+  JLLM_ERR_WORKSPACE = 5,         /* workspace missing, too small or misaligned */
+  JLLM_ERR_CUDA = 6,              /* a CUDA runtime/driver call failed         */
+  JLLM_ERR_DEVICE_TIMEOUT = 7,    /* a kernel-side bounded wait ran out        */
+  JLLM_ERR_NO_DEVICE = 8          /* the current device is not sm_103          */
+} jllm_status;
+
+typedef enum { JLLM_F32 = 0, JLLM_F16 = 1 } jllm_dtype;
+
+/* A cudaStream_t, passed as an opaque pointer. */
+typedef void* jllm_stream_t;
+
+/*
+ * jllm_q4k_dequant -- expand W to an [N,K] row-major matrix.
+ *   w_q4k  : W, [N][K/256] blocks (see layouts)
+ *   out    : [N][K] fp32 or fp16 (out_dt), 16-byte aligned
+ * Result is bit-exact to the rule under "numerics".
+ * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED, UNSUPPORTED_DTYPE, CUDA.
+ */
+jllm_status jllm_q4k_dequant(const void* w_q4k, void* out, jllm_dtype out_dt, int64_t N,
+                             int64_t K, jllm_stream_t stream);
+
+/*
+ * jllm_q4k_gemv -- decode matmul, M = 1: y[n] = sum_k x[k] * w[n,k].
+ * (the README's "INT4 dequant-fused GEMV", Kernels bullet)
+ *   w_q4k : W, [N][K/256] blocks
+ *   x     : [K] fp16
+ *   y     : [N] fp32
+ *   ws, ws_bytes : workspace, at least jllm_q4k_workspace_bytes(1, N, K)
+ *           bytes (may be NULL/0 when that is 0), 16-byte aligned
+ * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED, WORKSPACE, CUDA.
+ */
+jllm_status jllm_q4k_gemv(const void* w_q4k, const void* x, float* y, int64_t N, int64_t K,
+                          void* ws, size_t ws_bytes, jllm_stream_t stream);
+
+/*
+ * jllm_q4k_gemm -- Y[M,N] = X[M,K] * dequant(W)^T for any M >= 1.
+ * (the README's "tensor-core MMQ Q4_K prefill" for M above the GEMV
+ *  threshold, the GEMV kernel at or below it)
+ *   w_q4k : W, [N][K/256] blocks
+ *   x     : [M][K] fp16
+ *   y     : [M][N], fp32 or fp16 (y_dt)
+ *   ws, ws_bytes : workspace, at least jllm_q4k_workspace_bytes(M, N, K)
+ * M <= jllm_q4k_gemv_max_m() runs the GEMV kernel (gemm(M=1) == gemv);
+ * larger M runs the TMA + tcgen05 kernel (fp16 dequantised W, fp32
+ * accumulation in tensor memory).
+ * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED, UNSUPPORTED_DTYPE,
+ *         WORKSPACE, CUDA.
+ */
+jllm_status jllm_q4k_gemm(const void* w_q4k, const void* x, void* y, jllm_dtype y_dt, int64_t M,
+                          int64_t N, int64_t K, void* ws, size_t ws_bytes, jllm_stream_t stream);
+
+/*
+ * jllm_q4k_ffn_swiglu -- h = silu(X*Wg^T) * (X*Wu^T), the gate/up half of a
+ * SwiGLU MLP in one pass over X (the README's "fused ... SwiGLU", Kernels
+ * bullet).  silu(z) = z / (1 + e^-z).
+ *   w_gate, w_up : two Q4_K matrices, each [N][K/256] blocks
+ *   x     : [M][K] fp16
+ *   h     : [M][N] fp16
+ *   ws, ws_bytes : at least jllm_q4k_workspace_bytes(M, N, K) bytes
+ * g and u are each accurate to the matmul bound above; h is silu(g)*u
+ * evaluated in fp32 and rounded to fp16.
+ * Errors: as jllm_q4k_gemm.
+ */
+jllm_status jllm_q4k_ffn_swiglu(const void* w_gate, const void* w_up, const void* x, void* h,
+                                int64_t M, int64_t N, int64_t K, void* ws, size_t ws_bytes,
+                                jllm_stream_t stream);
+
+/* Workspace bytes that gemv/gemm/ffn_swiglu need for this shape (0 = none). */
+size_t jllm_q4k_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+/* Largest M that jllm_q4k_gemm sends to the GEMV kernel. */
+int jllm_q4k_gemv_max_m(void);
+
+/*
+ * Synchronise `stream`, then read and clear the device error word that a
+ * kernel sets when one of its bounded waits runs out.  Returns JLLM_OK,
+ * JLLM_ERR_DEVICE_TIMEOUT or JLLM_ERR_CUDA.
+ */
+jllm_status jllm_get_device_error(jllm_stream_t stream);
+
+/* Static, NUL-terminated name of a status code. */
+const char* jllm_status_string(jllm_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* JLLM_Q4K_H */

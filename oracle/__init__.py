@@ -209,3 +209,18 @@ def quantize(w: np.ndarray) -> np.ndarray:
 def tolerance(s: np.ndarray) -> np.ndarray:
     """The matmul's per-element bound: 2e-3 * S + 1e-5."""
     return 2e-3 * np.asarray(s, dtype=np.float64) + 1e-5
+
+
+def swiglu_tolerance(g: np.ndarray, u: np.ndarray, sg: np.ndarray, su: np.ndarray) -> np.ndarray:
+    """Per-element bound for a GPU h = fp16(silu(g') * u') whose g', u' each meet the matmul bound.
+
+    With Eg = tolerance(sg), Eu = tolerance(su) and |silu'| <= 1.1 everywhere:
+        |h' - silu(g)*u| <= 1.1*Eg*(|u| + Eu) + |silu(g)|*Eu + 2^-10*|silu(g)*u| + 1e-5
+    (the last two terms cover the fp32 evaluation and the rounding to fp16).
+    """
+    g = np.asarray(g, dtype=np.float64)
+    u = np.asarray(u, dtype=np.float64)
+    eg = tolerance(sg)
+    eu = tolerance(su)
+    sil = g / (1.0 + np.exp(-np.clip(g, -700, 700)))
+    return 1.1 * eg * (np.abs(u) + eu) + np.abs(sil) * eu + 2.0**-10 * np.abs(sil * u) + 1e-5

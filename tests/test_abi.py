@@ -1,0 +1,116 @@
+"""Host-side checks of the C ABI: the library builds for sm_103a, loads, exports
+every symbol include/jllm_q4k.h declares, and rejects bad arguments
+synchronously without touching CUDA.  No GPU needed."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "jllm_q4k.h")
+
+
+@pytest.fixture(scope="module")
+def q():
+    from bit_q4_weight_gb300 import _build
+
+    _build.build()
+    import bit_q4_weight_gb300
+
+    return bit_q4_weight_gb300
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(jllm_\w+)\s*\(", text)))
+
+
+def test_header_symbols_exported(q):
+    names = _declared()
+    assert set(names) == set(q.EXPORTS)
+    lib = ctypes.CDLL(q.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_library_targets_sm103a(q):
+    import subprocess
+
+    out = subprocess.run(["cuobjdump", "--list-elf", q.LIB_PATH], capture_output=True, text=True)
+    if out.returncode != 0:
+        pytest.skip("cuobjdump unavailable")
+    assert "sm_103a" in out.stdout
+
+
+def test_status_strings(q):
+    for code in range(9):
+        assert q.status_string(code).startswith("JLLM_")
+    assert q.status_string(99) == "JLLM_ERR_UNKNOWN"
+
+
+def test_workspace_and_threshold(q):
+    for shape in [(1, 1024, 2560), (33, 4096, 2560), (2048, 9728, 2560), (1, 151936, 2560)]:
+        assert q.jllm_q4k_workspace_bytes(*shape) >= 0
+    assert q.jllm_q4k_gemv_max_m() >= 0
+
+
+ALIGNED = 1 << 20  # a non-null, 16-byte-aligned fake address (never dereferenced)
+
+
+@pytest.mark.parametrize(
+    "args,status",
+    [
+        ((None, ALIGNED, ALIGNED, 0, 4, 128, 256, None, 0, None), 1),       # null W
+        ((ALIGNED, ALIGNED, ALIGNED, 0, 0, 128, 256, None, 0, None), 1),    # M = 0
+        ((ALIGNED, ALIGNED, ALIGNED, 0, 4, -1, 256, None, 0, None), 1),     # N < 1
+        ((ALIGNED, ALIGNED, ALIGNED, 0, 4, 128, 300, None, 0, None), 2),    # K % 256
+        ((ALIGNED, ALIGNED, ALIGNED, 0, 4, 128, 0, None, 0, None), 2),      # K = 0
+        ((ALIGNED, ALIGNED, ALIGNED, 0, 4, 128, 1 << 40, None, 0, None), 2),  # K too large
+        ((ALIGNED, ALIGNED, ALIGNED, 7, 4, 128, 256, None, 0, None), 4),    # dtype
+        ((ALIGNED + 8, ALIGNED, ALIGNED, 0, 4, 128, 256, None, 0, None), 3),  # W misaligned
+        ((ALIGNED, ALIGNED + 2, ALIGNED, 0, 4, 128, 256, None, 0, None), 3),  # X misaligned
+        ((ALIGNED, ALIGNED, ALIGNED + 4, 1, 4, 128, 256, None, 0, None), 3),  # Y misaligned
+    ],
+)
+def test_gemm_argument_errors(q, args, status):
+    assert q.lib.jllm_q4k_gemm(*args) == status
+
+
+def test_other_entry_argument_errors(q):
+    A = ALIGNED
+    assert q.lib.jllm_q4k_dequant(None, A, 0, 4, 256, None) == 1
+    assert q.lib.jllm_q4k_dequant(A, A, 2, 4, 256, None) == 4
+    assert q.lib.jllm_q4k_dequant(A, A, 0, 4, 255, None) == 2
+    assert q.lib.jllm_q4k_dequant(A + 1, A, 0, 4, 256, None) == 3
+    assert q.lib.jllm_q4k_gemv(A, None, A, 4, 256, None, 0, None) == 1
+    assert q.lib.jllm_q4k_gemv(A, A, A, 4, 512 + 7, None, 0, None) == 2
+    assert q.lib.jllm_q4k_gemv(A, A, A + 8, 4, 512, None, 0, None) == 3
+    assert q.lib.jllm_q4k_ffn_swiglu(A, None, A, A, 1, 4, 256, None, 0, None) == 1
+    assert q.lib.jllm_q4k_ffn_swiglu(A, A, A, A, 1, 4, 100, None, 0, None) == 2
+    assert q.lib.jllm_q4k_ffn_swiglu(A, A + 4, A, A, 1, 4, 256, None, 0, None) == 3
+
+
+def _no_cuda():
+    try:
+        import torch
+
+        return not torch.cuda.is_available()
+    except Exception:
+        return True
+
+
+@pytest.mark.skipif(not _no_cuda(), reason="only meaningful where no CUDA device exists")
+def test_valid_call_without_device_reports_error(q):
+    # With valid arguments and no device the call must fail cleanly, never crash.
+    st = q.lib.jllm_q4k_gemm(ALIGNED, ALIGNED, ALIGNED, 0, 4, 128, 256, None, 0, None)
+    assert st in (q.JLLM_ERR_CUDA, q.JLLM_ERR_NO_DEVICE)
+
+
+def test_python_wrappers_validate_tensors(q):
+    torch = pytest.importorskip("torch")
+    w = torch.zeros((4, 144), dtype=torch.uint8)
+    x = torch.zeros((1, 256), dtype=torch.float16)
+    with pytest.raises(ValueError):
+        q.jllm_q4k_gemm(w, x, 4, 256)  # CPU tensors are rejected before any call
