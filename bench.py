@@ -118,17 +118,19 @@ def build_inputs(torch, dev, layers):
 
 
 def time_graph(torch, graph, stream, steps, warmup):
-    for _ in range(warmup):
-        graph.replay()
-    torch.cuda.synchronize()
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
-    start.record(stream)
-    for _ in range(steps):
-        graph.replay()
-    end.record(stream)
+    """Seconds per replay, CUDA events recorded on the stream the graph is launched on."""
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            graph.replay()
+        torch.cuda.synchronize()
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for _ in range(steps):
+            graph.replay()
+        end.record(stream)
     end.synchronize()
-    return start.elapsed_time(end) / 1e3 / steps  # seconds per step
+    return start.elapsed_time(end) / 1e3 / steps
 
 
 def run_ours(args):

@@ -13,9 +13,9 @@ HEADER = os.path.join(ROOT, "include", "jllm_q4k.h")
 
 @pytest.fixture(scope="module")
 def q():
-    from bit_q4_weight_gb300 import _build
+    import __graft_entry__
 
-    _build.build()
+    __graft_entry__.build()
     import bit_q4_weight_gb300
 
     return bit_q4_weight_gb300

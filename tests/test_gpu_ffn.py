@@ -71,12 +71,11 @@ def test_ffn_block(q, weights, M):
         g, _ = oracle.matmul(weights["gate"], x[: min(M, 8)], F, H)
         u, _ = oracle.matmul(weights["up"], x[: min(M, 8)], F, H)
         h16 = oracle.swiglu(g, u).astype(np.float16)
-    Md = h16.shape[0]
-    y = q.jllm_q4k_gemm(dev(weights["down"]), dev(h16), H, F,
-                        out_dtype=torch.float32 if Md == 1 else torch.float16).float().cpu().numpy()
+    # fp32 output: with these unnormalised synthetic magnitudes |y| reaches ~2.5e5,
+    # beyond the fp16 range.
+    y = q.jllm_q4k_gemm(dev(weights["down"]), dev(h16), H, F, out_dtype=torch.float32).cpu().numpy()
     ref, s = oracle.matmul(weights["down"], h16, H, F)
-    extra = 0.0 if Md == 1 else 2.0**-11 * np.abs(ref) + 2.0**-24
-    assert np.all(np.abs(y - ref) <= oracle.tolerance(s) + extra)
+    assert_within(y, ref, s, f"down M={h16.shape[0]}")
 
 
 @pytest.mark.parametrize("M", [1, 512])
