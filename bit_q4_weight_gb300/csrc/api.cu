@@ -167,10 +167,11 @@ jllm_status jllm_q4k_ffn_swiglu(const void* w_gate, const void* w_up, const void
 }
 
 jllm_status jllm_get_device_error(jllm_stream_t stream) {
-  uint32_t bits = 0;
-  cudaError_t e = jllm::read_clear_gemm_error(&bits, (cudaStream_t)stream);
+  uint32_t a = 0, b = 0;
+  cudaError_t e = jllm::read_clear_gemm_error(&a, (cudaStream_t)stream);
+  if (e == cudaSuccess) e = jllm::read_clear_gemv_error(&b);
   if (e != cudaSuccess) return JLLM_ERR_CUDA;
-  return bits ? JLLM_ERR_DEVICE_TIMEOUT : JLLM_OK;
+  return (a | b) ? JLLM_ERR_DEVICE_TIMEOUT : JLLM_OK;
 }
 
 }  // extern "C"

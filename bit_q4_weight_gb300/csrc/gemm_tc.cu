@@ -10,22 +10,25 @@
 // weight is dequantised once per CTA and reused for BN tokens.  D lives in
 // tensor memory (lane = weight row, column = token, fp32).
 //
-// Roles (192 threads):
+// Roles (320 threads):
 //   warp 0  TMA producer: per 64-wide K step one X tile {64 k x BN tokens},
 //           128-byte swizzled; per 256-wide block one raw W tile
 //           {144 bytes x 1 block x 128 rows} through a 3-D byte view of W.
 //   warp 1  TMEM allocation and the MMA issuer (one thread): four
 //           tcgen05.mma (K = 16 each) per K step, tcgen05.commit frees the
 //           stages.
-//   warps 2-5  dequantisers, one weight row per thread: read the row's header
-//           and 32 code bytes from the raw tile, form 64 values
-//           (d*sc)*q - dmin*m in fp32 (exactly the fp32 dequant), round to
-//           fp16 and store them in the 128-byte-swizzle K-major layout the MMA
-//           descriptor expects.  They then run the epilogue: tcgen05.ld of
-//           their 32 TMEM lanes, store Y (fp32 / fp16) or silu(g)*u (fp16).
+//   warps 2-9  dequantisers, two threads per weight row (low / high nibbles
+//           of the row's 32 code bytes for this step): form the 32 values
+//           (d*sc)*q - dmin*m exactly as the fp32 dequant does (sc*q exactly
+//           in fp16x2, then one fp32 fma per value), round to fp16 and store
+//           them in the 128-byte-swizzle K-major layout the MMA descriptor
+//           expects.  They then run the epilogue: tcgen05.ld of their 32 TMEM
+//           lanes, store Y (fp32 / fp16) or silu(g)*u (fp16).
 // Every wait is bounded; a wait that runs out sets the device error word and
 // the CTA winds down (pending copies and MMAs are awaited, TMEM is freed).
 #include <cudaTypedefs.h>
+
+#include <stdlib.h>
 
 #include <mutex>
 
@@ -36,6 +39,26 @@ namespace jllm {
 namespace {
 
 __device__ uint32_t g_gemm_error;
+
+__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t mask, uint32_t orv) {
+  uint32_t r;
+  asm("lop3.b32 %0, %1, %2, %3, 0xea;" : "=r"(r) : "r"(a), "r"(mask), "r"(orv));  // (a & b) | c
+  return r;
+}
+
+// Two dequantised fp16 weights from two offset codes h (fp16x2):
+// p = h*scv + offv = sc*q (exact), w = fma(d, p, nt) in fp32, packed to fp16x2.
+__device__ __forceinline__ uint32_t dq_pair(uint32_t h2, uint32_t scv, uint32_t offv, unsigned short d,
+                                            float nt) {
+  uint32_t p, out;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(p) : "r"(h2), "r"(scv), "r"(offv));
+  asm("{\n .reg .b16 pl, ph;\n .reg .f32 a, b;\n mov.b32 {pl, ph}, %1;\n"
+      " fma.rn.f32.f16 a, %2, pl, %3;\n fma.rn.f32.f16 b, %2, ph, %3;\n"
+      " cvt.rn.f16x2.f32 %0, b, a;\n}"
+      : "=r"(out)
+      : "r"(p), "h"(d), "f"(nt));
+  return out;
+}
 
 constexpr int TILE_N = 128;           // weight rows per CTA (MMA M)
 constexpr int KSTEP = 64;             // K per stage (128 bytes of fp16)
@@ -54,7 +77,7 @@ struct GemmParams {
 };
 
 template <bool SWIGLU>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     q4k_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW0,
                        const __grid_constant__ CUtensorMap tmW1, const GemmParams p) {
   constexpr int NMAT = SWIGLU ? 2 : 1;
@@ -83,10 +106,10 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int i = 0; i < p.SW; ++i) {
       mbar_init(b_wfull + 8 * i, 1);
-      mbar_init(b_wempty + 8 * i, 4);
+      mbar_init(b_wempty + 8 * i, 8);
     }
     for (int i = 0; i < p.SA; ++i) {
-      mbar_init(b_afull + 8 * i, 4);
+      mbar_init(b_afull + 8 * i, 8);
       mbar_init(b_aempty + 8 * i, 1);
     }
     mbar_init(b_acc, 1);
@@ -168,7 +191,12 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else {
     // ------------------------------------------------- dequant + epilogue --
-    const int q = warp & 3;       // TMEM lane quarter this warp may access
+    // Warps 2..9: warp w handles TMEM lane quarter q = w & 3 (rows 32q..32q+31)
+    // and nibble side hs = (w - 2) >> 2: hs = 0 makes sub-block 2c (low
+    // nibbles, k 0..31 of the step), hs = 1 sub-block 2c+1 (high nibbles,
+    // k 32..63).
+    const int q = warp & 3;
+    const int hs = (warp - 2) >> 2;
     const int r = 32 * q + lane;  // weight row within the tile
     bool ok = true;
     for (int ks = 0; ks < KS && ok; ++ks) {
@@ -183,32 +211,35 @@ __global__ void __launch_bounds__(192, 1)
         const uint4 hd = *reinterpret_cast<const uint4*>(raw);
         const uint4 q0 = *reinterpret_cast<const uint4*>(raw + 16 + 32 * c);
         const uint4 q1 = *reinterpret_cast<const uint4*>(raw + 32 + 32 * c);
-        uint32_t sc_lo, m_lo, sc_hi, m_hi;
-        q4k_scale_min(hd.y, hd.z, hd.w, 2 * c, sc_lo, m_lo);
-        q4k_scale_min(hd.y, hd.z, hd.w, 2 * c + 1, sc_hi, m_hi);
-        const float dd = half_lo_to_float(hd.x), dm = half_hi_to_float(hd.x);
-        const float s_lo = __fmul_rn(dd, (float)sc_lo), t_lo = __fmul_rn(dm, (float)m_lo);
-        const float s_hi = __fmul_rn(dd, (float)sc_hi), t_hi = __fmul_rn(dm, (float)m_hi);
+        uint32_t sc, m;
+        q4k_scale_min(hd.y, hd.z, hd.w, 2 * c + hs, sc, m);
+        // p = sc*q exactly in fp16 from the offset code h (1024+q or 1024+16q):
+        //   p = h*sc - 1024*sc  or  p = h*(sc/16) - 64*sc   (one rounding of an
+        //   exact integer <= 945).  Then w = fma(d, p, -dmin*m) in fp32 is the
+        //   exact value rounded once, i.e. the fp32 dequant, rounded to fp16.
+        const __half sch = __uint2half_rn(sc);
+        const __half2 scv = __half2half2(hs ? __hmul(sch, __float2half(0.0625f)) : sch);
+        const __half2 offv = __half2half2(__hmul(sch, __float2half(hs ? -64.f : -1024.f)));
+        const uint32_t scv_u = *reinterpret_cast<const uint32_t*>(&scv);
+        const uint32_t offv_u = *reinterpret_cast<const uint32_t*>(&offv);
+        const unsigned short d16 = (unsigned short)(hd.x & 0xffffu);
+        const float nt = -__fmul_rn(half_hi_to_float(hd.x), (float)m);
+        const uint32_t mask = hs ? 0x00F000F0u : 0x000F000Fu;
         const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
         uint8_t* arow = smem + p.off_a + (size_t)(s_a * NMAT + mat) * A_STAGE_BYTES + (size_t)r * 128;
 #pragma unroll
-        for (int j8 = 0; j8 < 8; ++j8) {
-          // 16-byte chunk j8 holds k = 8*j8 .. 8*j8+7 of this 64-wide step:
-          // j8 < 4: low nibbles of code bytes 8*j8.., sub-block 2c;
-          // j8 >= 4: high nibbles of code bytes 8*(j8-4).., sub-block 2c+1.
-          const bool high = j8 >= 4;
-          const uint32_t w0 = qw[2 * (j8 & 3)], w1 = qw[2 * (j8 & 3) + 1];
-          const float s = high ? s_hi : s_lo, t = high ? t_hi : t_lo;
+        for (int jj = 0; jj < 4; ++jj) {
+          // output chunk j8 = 4*hs + jj holds k = 8*j8..8*j8+7: code bytes 8*jj..8*jj+7
           uint32_t pk[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const uint32_t word = e < 2 ? w0 : w1;
-            const uint32_t b0 = (word >> (16 * (e & 1))) & 0xffu, b1 = (word >> (16 * (e & 1) + 8)) & 0xffu;
-            const uint32_t qa = high ? (b0 >> 4) : (b0 & 15u), qb = high ? (b1 >> 4) : (b1 & 15u);
-            const __half ha = __float2half_rn(q4k_value(s, t, qa));
-            const __half hb = __float2half_rn(q4k_value(s, t, qb));
-            pk[e] = (uint32_t)__half_as_ushort(ha) | ((uint32_t)__half_as_ushort(hb) << 16);
+          for (int e = 0; e < 2; ++e) {
+            const uint32_t w = qw[2 * jj + e];
+            uint32_t wp;
+            asm("prmt.b32 %0, %1, 0, 0x3120;" : "=r"(wp) : "r"(w));  // bytes b0 b2 b1 b3
+            pk[2 * e] = dq_pair(lop3_and_or(wp, mask, 0x64006400u), scv_u, offv_u, d16, nt);       // k, k+1
+            pk[2 * e + 1] = dq_pair(lop3_and_or(wp >> 8, mask, 0x64006400u), scv_u, offv_u, d16, nt);  // k+2, k+3
           }
+          const int j8 = 4 * hs + jj;
           *reinterpret_cast<uint4*>(arow + ((j8 ^ (r & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
       }
@@ -226,7 +257,8 @@ __global__ void __launch_bounds__(192, 1)
       tc_fence_after();
       const int n = n0 + r;
       const uint32_t lane_addr = tmem + ((uint32_t)(32 * q) << 16);
-      for (int cc = 0; cc < p.BN; cc += 32) {
+      // the two warps of a lane quarter split the token columns in 32-wide chunks
+      for (int cc = 32 * hs; cc < p.BN; cc += 64) {
         uint32_t v[32];
         tmem_ld32(lane_addr + cc, v);
         if (SWIGLU) {
@@ -237,7 +269,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
               const int m = m0 + cc + j;
-              if (m < p.M) {
+              if (m < p.M && cc + j < p.BN) {
                 const float g = __uint_as_float(v[j]), uu = __uint_as_float(u[j]);
                 y[(size_t)m * p.N + n] = __float2half_rn(g / (1.0f + expf(-g)) * uu);
               }
@@ -249,14 +281,14 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
               const int m = m0 + cc + j;
-              if (m < p.M) y[(size_t)m * p.N + n] = __float2half_rn(__uint_as_float(v[j]));
+              if (m < p.M && cc + j < p.BN) y[(size_t)m * p.N + n] = __float2half_rn(__uint_as_float(v[j]));
             }
           } else {
             float* y = reinterpret_cast<float*>(p.y);
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
               const int m = m0 + cc + j;
-              if (m < p.M) y[(size_t)m * p.N + n] = __uint_as_float(v[j]);
+              if (m < p.M && cc + j < p.BN) y[(size_t)m * p.N + n] = __uint_as_float(v[j]);
             }
           }
         }
@@ -325,7 +357,7 @@ cudaError_t launch_tc(const CUtensorMap& mx, const CUtensorMap& mw0, const CUten
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)((N + TILE_N - 1) / TILE_N), (unsigned)((p.M + p.BN - 1) / p.BN));
-  kern<<<grid, 192, smem, s>>>(mx, mw0, mw1, p);
+  kern<<<grid, 320, smem, s>>>(mx, mw0, mw1, p);
   return cudaGetLastError();
 }
 
@@ -338,8 +370,14 @@ cudaError_t launch_gemm_tc(const void* w0, const void* w1, const void* x, void* 
   const int nmat = swiglu ? 2 : 1;
   if (M > INT32_MAX / 2 || N > INT32_MAX / 2 || K / QK > INT32_MAX / 8) return cudaErrorInvalidValue;
   // Tokens per CTA: the whole of M up to 256 (rounded up to 16), else 256
-  // (128 when the SwiGLU epilogue needs two accumulators).
-  const int bn_cap = swiglu ? 128 : 256;
+  // (128 when the SwiGLU epilogue needs two accumulators).  Stage counts:
+  // raw-W and dequantised-A rings first, the rest of shared memory for X.
+  // JLLM_GEMM_BN / _SA / _SW override (tuning).
+  static const int env_bn = getenv("JLLM_GEMM_BN") ? atoi(getenv("JLLM_GEMM_BN")) : 0;
+  static const int env_sa = getenv("JLLM_GEMM_SA") ? atoi(getenv("JLLM_GEMM_SA")) : 0;
+  static const int env_sw = getenv("JLLM_GEMM_SW") ? atoi(getenv("JLLM_GEMM_SW")) : 0;
+  int bn_cap = swiglu ? 128 : 256;
+  if (env_bn >= 16 && env_bn <= bn_cap && env_bn % 16 == 0) bn_cap = env_bn;
   int BN = (int)((M + 15) / 16 * 16);
   if (BN > bn_cap) BN = bn_cap;
   uint32_t cols = 32;
@@ -353,11 +391,15 @@ cudaError_t launch_gemm_tc(const void* w0, const void* w1, const void* x, void* 
   p.BN = BN;
   p.tmem_cols = cols;
   p.out_f16 = (y_f16 || swiglu) ? 1 : 0;
-  p.SW = 2;
-  p.SA = 2;
+  p.SW = env_sw > 0 ? env_sw : 3;
+  p.SA = env_sa > 0 ? env_sa : 3;
   const size_t x_stage = (size_t)BN * KSTEP * 2;
   const size_t budget = dev.smem_optin - 1024 /*alignment*/ - 512 /*barriers*/;
-  const size_t fixed = (size_t)p.SW * W_STAGE_BYTES * nmat + (size_t)p.SA * A_STAGE_BYTES * nmat;
+  size_t fixed = (size_t)p.SW * W_STAGE_BYTES * nmat + (size_t)p.SA * A_STAGE_BYTES * nmat;
+  while (fixed + 2 * x_stage > budget && (p.SW > 2 || p.SA > 2)) {
+    if (p.SW >= p.SA && p.SW > 2) --p.SW; else --p.SA;
+    fixed = (size_t)p.SW * W_STAGE_BYTES * nmat + (size_t)p.SA * A_STAGE_BYTES * nmat;
+  }
   if (fixed + 2 * x_stage > budget) return cudaErrorInvalidValue;
   size_t sxn = (budget - fixed) / x_stage;
   if (sxn > 8) sxn = 8;

@@ -33,7 +33,9 @@ cudaError_t launch_gemv(const void* w0, const void* w1, const void* x, void* y, 
 cudaError_t launch_gemm_tc(const void* w0, const void* w1, const void* x, void* y, bool y_f16, int64_t M,
                            int64_t N, int64_t K, cudaStream_t s);
 
-// Read and clear the device error word of the tcgen05 kernels.
+// Read and clear the device error word of the tcgen05 kernels (after
+// synchronising the stream) and of the GEMV kernels.
 cudaError_t read_clear_gemm_error(uint32_t* bits, cudaStream_t s);
+cudaError_t read_clear_gemv_error(uint32_t* bits);
 
 }  // namespace jllm
