@@ -125,14 +125,33 @@ def _w_shape(N: int, K: int):
     return (N, K // QK * BLOCK_BYTES)
 
 
-def _ws(M, N, K, ws, device):
+# Zero-filled workspaces kept per (device, stream): the library returns a
+# workspace to its reusable state after every call, and calls on one stream
+# are ordered, so one buffer per stream suffices.
+_WS_CACHE = {}
+
+
+def _ws(M, N, K, ws, device, stream):
     need = int(lib.jllm_q4k_workspace_bytes(M, N, K))
-    if need == 0:
+    if need == 0 or ws is False:  # ws=False: run without a workspace
         return None, 0
     torch = _torch()
     if ws is None:
-        ws = torch.empty(need, dtype=torch.uint8, device=device)
+        key = (device.index if device.index is not None else torch.cuda.current_device(), _stream_ptr(stream))
+        ws = _WS_CACHE.get(key)
+        if ws is None or ws.numel() < need:
+            ws = torch.zeros(need, dtype=torch.uint8, device=device)
+            _WS_CACHE[key] = ws
     return ws, ws.numel() * ws.element_size()
+
+
+def workspace(M: int, N: int, K: int, device=None):
+    """A zero-filled workspace tensor for gemm/ffn_swiglu of this shape (None if none is used)."""
+    torch = _torch()
+    need = int(lib.jllm_q4k_workspace_bytes(M, N, K))
+    if need == 0:
+        return None
+    return torch.zeros(need, dtype=torch.uint8, device=device or "cuda")
 
 
 # ------------------------------------------------------------------ the API --
@@ -175,7 +194,7 @@ def jllm_q4k_gemv(w, x, N: int, K: int, out=None, ws=None, stream=None):
     if out is None:
         out = torch.empty((N,), dtype=torch.float32, device=w.device)
     _need(out, torch.float32, (N,), "out")
-    ws, nbytes = _ws(1, N, K, ws, w.device)
+    ws, nbytes = _ws(1, N, K, ws, w.device, stream)
     _check(
         lib.jllm_q4k_gemv(w.data_ptr(), x.data_ptr(), out.data_ptr(), N, K,
                           ws.data_ptr() if ws is not None else None, nbytes, _stream_ptr(stream)),
@@ -198,7 +217,7 @@ def jllm_q4k_gemm(w, x, N: int, K: int, out_dtype=None, out=None, ws=None, strea
     if out is None:
         out = torch.empty((M, N), dtype=out_dtype, device=w.device)
     _need(out, out_dtype, (M, N), "out")
-    ws, nbytes = _ws(M, N, K, ws, w.device)
+    ws, nbytes = _ws(M, N, K, ws, w.device, stream)
     dt = JLLM_F16 if out_dtype == torch.float16 else JLLM_F32
     _check(
         lib.jllm_q4k_gemm(w.data_ptr(), x.data_ptr(), out.data_ptr(), dt, M, N, K,
@@ -220,7 +239,7 @@ def jllm_q4k_ffn_swiglu(w_gate, w_up, x, N: int, K: int, out=None, ws=None, stre
     if out is None:
         out = torch.empty((M, N), dtype=torch.float16, device=x.device)
     _need(out, torch.float16, (M, N), "out")
-    ws, nbytes = _ws(M, N, K, ws, x.device)
+    ws, nbytes = _ws(M, N, K, ws, x.device, stream)
     _check(
         lib.jllm_q4k_ffn_swiglu(w_gate.data_ptr(), w_up.data_ptr(), x.data_ptr(), out.data_ptr(), M, N, K,
                                 ws.data_ptr() if ws is not None else None, nbytes, _stream_ptr(stream)),

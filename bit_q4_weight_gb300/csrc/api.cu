@@ -59,9 +59,11 @@ jllm_status check_shape(int64_t M, int64_t N, int64_t K) {
   return JLLM_OK;
 }
 
+// The workspace is optional: NULL runs without it; a given one must be
+// large enough and aligned.
 jllm_status check_workspace(void* ws, size_t ws_bytes, size_t need) {
-  if (need == 0) return JLLM_OK;
-  if (ws == nullptr || ws_bytes < need || !aligned16(ws)) return JLLM_ERR_WORKSPACE;
+  if (ws == nullptr || need == 0) return JLLM_OK;
+  if (ws_bytes < need || ((uintptr_t)ws & 255u) != 0) return JLLM_ERR_WORKSPACE;
   return JLLM_OK;
 }
 
@@ -110,10 +112,8 @@ const char* jllm_status_string(jllm_status status) {
 int jllm_q4k_gemv_max_m(void) { return gemv_max_m(); }
 
 size_t jllm_q4k_workspace_bytes(int64_t M, int64_t N, int64_t K) {
-  (void)M;
-  (void)N;
-  (void)K;
-  return 0;
+  if (check_shape(M, N, K) != JLLM_OK || M <= gemv_max_m()) return 0;
+  return jllm::gemm_workspace_bytes();
 }
 
 jllm_status jllm_q4k_dequant(const void* w_q4k, void* out, jllm_dtype out_dt, int64_t N, int64_t K,
@@ -150,7 +150,7 @@ jllm_status jllm_q4k_gemm(const void* w_q4k, const void* x, void* y, jllm_dtype 
   cudaStream_t s = (cudaStream_t)stream;
   if (M <= gemv_max_m() && y_dt == JLLM_F32)
     return from_cuda(jllm::launch_gemv(w_q4k, nullptr, x, y, N, K, s));
-  return from_cuda(jllm::launch_gemm_tc(w_q4k, nullptr, x, y, y_dt == JLLM_F16, M, N, K, s));
+  return from_cuda(jllm::launch_gemm_tc(w_q4k, nullptr, x, y, y_dt == JLLM_F16, M, N, K, ws, ws_bytes, s));
 }
 
 jllm_status jllm_q4k_ffn_swiglu(const void* w_gate, const void* w_up, const void* x, void* h, int64_t M,
@@ -163,7 +163,7 @@ jllm_status jllm_q4k_ffn_swiglu(const void* w_gate, const void* w_up, const void
   if ((st = check_device()) != JLLM_OK) return st;
   cudaStream_t s = (cudaStream_t)stream;
   if (M <= gemv_max_m()) return from_cuda(jllm::launch_gemv(w_gate, w_up, x, h, N, K, s));
-  return from_cuda(jllm::launch_gemm_tc(w_gate, w_up, x, h, true, M, N, K, s));
+  return from_cuda(jllm::launch_gemm_tc(w_gate, w_up, x, h, true, M, N, K, ws, ws_bytes, s));
 }
 
 jllm_status jllm_get_device_error(jllm_stream_t stream) {

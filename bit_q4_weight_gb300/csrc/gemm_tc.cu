@@ -7,25 +7,37 @@
 // Orientation.  The MMA computes D[128 weight rows][BN tokens] += A * B^T with
 // A = the dequantised fp16 weight tile (M = 128 rows of W, K-major) and B = a
 // tile of X (N = BN tokens, K-major).  Putting W on the MMA's M side means a
-// weight is dequantised once per CTA and reused for BN tokens.  D lives in
+// weight is dequantised once per tile and reused for BN tokens.  D lives in
 // tensor memory (lane = weight row, column = token, fp32).
 //
-// Roles (320 threads):
-//   warp 0  TMA producer: per 64-wide K step one X tile {64 k x BN tokens},
-//           128-byte swizzled; per 256-wide block one raw W tile
-//           {144 bytes x 1 block x 128 rows} through a 3-D byte view of W.
-//   warp 1  TMEM allocation and the MMA issuer (one thread): four
-//           tcgen05.mma (K = 16 each) per K step, tcgen05.commit frees the
-//           stages.
-//   warps 2-9  dequantisers, two threads per weight row (low / high nibbles
-//           of the row's 32 code bytes for this step): form the 32 values
-//           (d*sc)*q - dmin*m exactly as the fp32 dequant does (sc*q exactly
-//           in fp16x2, then one fp32 fma per value), round to fp16 and store
-//           them in the 128-byte-swizzle K-major layout the MMA descriptor
-//           expects.  They then run the epilogue: tcgen05.ld of their 32 TMEM
-//           lanes, store Y (fp32 / fp16) or silu(g)*u (fp16).
-// Every wait is bounded; a wait that runs out sets the device error word and
-// the CTA winds down (pending copies and MMAs are awaited, TMEM is freed).
+// Persistent schedule.  One CTA per SM walks a contiguous range of "units":
+// the K steps (64 wide) of the tiles laid out tile after tile.  Without a
+// workspace a range is a whole number of tiles.  With one (stream-K), the
+// ranges are equal in K steps, so the last wave of tiles is shared out
+// evenly; a tile cut between CTAs is finished by the CTA that owns its first
+// K step, which adds the fp32 partial sums the later CTAs left in the
+// workspace, in CTA order (deterministic).
+//
+// Roles (448 threads):
+//   warp 0      TMA producer: per K step one X tile {64 k x BN tokens},
+//               128-byte swizzled; per 256-wide block one raw W tile
+//               {144 bytes x 1 block x 128 rows} through a 3-D byte view.
+//   warp 1      TMEM owner (512 columns = two accumulator buffers) and MMA
+//               issuer (one thread): four tcgen05.mma (K = 16) per K step,
+//               tcgen05.commit frees the stages and, per unit, hands the
+//               accumulator buffer to the epilogue.
+//   warps 2-9   dequantisers, two threads per weight row (low / high nibbles
+//               of the row's 32 code bytes for the step): the values
+//               (d*sc)*q - dmin*m exactly as the fp32 dequant forms them,
+//               rounded to fp16, stored in the 128-byte-swizzle K-major
+//               layout the MMA descriptor reads.
+//   warps 10-13 epilogue: tcgen05.ld of one TMEM lane quarter, store Y
+//               (fp32 / fp16) or silu(g)*u (fp16), or the fp32 partial of a
+//               cut tile.  It runs while the MMA fills the other buffer.
+// Ring positions advance by counters (stage, phase), never by division.
+// Every wait is bounded; a wait that runs out sets the device error word
+// and the CTA winds down (copies and MMAs in flight are awaited, TMEM is
+// freed).
 #include <cudaTypedefs.h>
 
 #include <stdlib.h>
@@ -60,246 +72,429 @@ __device__ __forceinline__ uint32_t dq_pair(uint32_t h2, uint32_t scv, uint32_t 
   return out;
 }
 
-constexpr int TILE_N = 128;           // weight rows per CTA (MMA M)
-constexpr int KSTEP = 64;             // K per stage (128 bytes of fp16)
-constexpr int A_STAGE_BYTES = TILE_N * KSTEP * 2;        // 16 KiB
-constexpr int W_STAGE_BYTES = TILE_N * BLOCK_BYTES;      // 18 KiB
-constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;        // 2 s
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t atom_add_release_gpu(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.add.release.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+__device__ __forceinline__ uint32_t atom_add_acqrel_gpu(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+constexpr int TILE_N = 128;                         // weight rows per tile (MMA M)
+constexpr int KSTEP = 64;                           // K per stage (128 bytes of fp16)
+constexpr int A_STAGE_BYTES = TILE_N * KSTEP * 2;   // 16 KiB
+constexpr int W_STAGE_BYTES = TILE_N * BLOCK_BYTES; // 18 KiB
+constexpr int NUM_THREADS = 448;
+constexpr int EPI_WARP0 = 10;                       // warps 10..13
+constexpr int NUM_EPI_WARPS = 4;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t ACC_COLS = 256;                  // TMEM columns per accumulator buffer
+constexpr int SLOT_FLOATS = TILE_N * 256;           // fp32 partial of one tile (128 KiB)
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;   // 2 s
+
+template <bool SWIGLU>
+struct Cfg {
+  static constexpr int NMAT = SWIGLU ? 2 : 1;  // weight matrices per tile
+  static constexpr int SX = 3;                 // X ring
+  static constexpr int SA = SWIGLU ? 3 : 4;    // dequantised-A ring
+  static constexpr int SW = SWIGLU ? 2 : 3;    // raw-W ring
+  static constexpr int BN_MAX = SWIGLU ? 128 : 256;
+  static constexpr int NBARS = 2 * (SX + SA + SW) + 2 + 2 + 1;
+};
 
 struct GemmParams {
-  void* y;
+  void* y;               // [M][N] fp32 / fp16 (h for SwiGLU)
+  float* partial;        // stream-K slots, SLOT_FLOATS per CTA (nullptr: whole tiles only)
+  uint32_t* flags;       // one counter per CTA next to the slots
   int M, N, NB;
-  int BN;          // tokens per CTA (MMA N), multiple of 16, <= 256
-  int SX, SA, SW;  // stage counts of the X, A and raw-W rings
-  uint32_t off_x, off_a, off_w, off_bar;  // shared-memory carve-up (bytes)
-  uint32_t tmem_cols;
+  int BN;                // tokens per tile, multiple of 16
+  int m_tiles;           // ceil(M / BN)
+  int KS;                // K steps per tile (4 per super-block)
+  long long grains;      // units / grain
+  int grain;             // KS (whole tiles) or 1 (stream-K)
+  uint32_t x_stage_bytes;
+  uint32_t off_x, off_a, off_w, off_bar;
   int out_f16;
 };
 
+// Stage index and phase parity of a ring of S stages.
+template <int S>
+struct Ring {
+  int s = 0;
+  uint32_t ph = 0;
+  __device__ __forceinline__ void next() {
+    if (++s == S) {
+      s = 0;
+      ph ^= 1u;
+    }
+  }
+};
+
+__device__ __forceinline__ long long range_start(const GemmParams& p, long long g) {
+  return (g * p.grains / gridDim.x) * p.grain;
+}
+
+// Walks the units of one CTA's range: tile, and its K steps [k0, k1).
+struct UnitIter {
+  long long u, end;
+  int KS;
+  int tile = 0, k0 = 0, k1 = 0;
+  __device__ __forceinline__ bool next() {
+    if (u >= end) return false;
+    tile = (int)(u / KS);
+    k0 = (int)(u - (long long)tile * KS);
+    const long long rem = end - u;
+    k1 = rem < (long long)(KS - k0) ? k0 + (int)rem : KS;
+    u += k1 - k0;
+    return true;
+  }
+};
+
 template <bool SWIGLU>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(NUM_THREADS, 1)
     q4k_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW0,
                        const __grid_constant__ CUtensorMap tmW1, const GemmParams p) {
-  constexpr int NMAT = SWIGLU ? 2 : 1;
+  using C = Cfg<SWIGLU>;
+  constexpr int NMAT = C::NMAT, SX = C::SX, SA = C::SA, SW = C::SW;
   extern __shared__ uint8_t gemm_smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(gemm_smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   const uint32_t sx = sbase + p.off_x, sa = sbase + p.off_a, sw = sbase + p.off_w;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.off_bar);
-  // barrier layout: x_full[SX] x_empty[SX] w_full[SW] w_empty[SW] a_full[SA] a_empty[SA] acc_full
-  const uint32_t b_xfull = smem_u32(bars), b_xempty = b_xfull + 8 * p.SX;
-  const uint32_t b_wfull = b_xempty + 8 * p.SX, b_wempty = b_wfull + 8 * p.SW;
-  const uint32_t b_afull = b_wempty + 8 * p.SW, b_aempty = b_afull + 8 * p.SA;
-  const uint32_t b_acc = b_aempty + 8 * p.SA;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * (p.SX + p.SW + p.SA) + 1);
+  // barriers: x_full[SX] x_empty[SX] a_full[SA] a_empty[SA] w_full[SW] w_empty[SW]
+  //           acc_full[2] acc_empty[2] drain
+  const uint32_t b_xfull = sbase + p.off_bar, b_xempty = b_xfull + 8 * SX;
+  const uint32_t b_afull = b_xempty + 8 * SX, b_aempty = b_afull + 8 * SA;
+  const uint32_t b_wfull = b_aempty + 8 * SA, b_wempty = b_wfull + 8 * SW;
+  const uint32_t b_accfull = b_wempty + 8 * SW, b_accempty = b_accfull + 16, b_drain = b_accempty + 16;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + p.off_bar + 8 * C::NBARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n0 = blockIdx.x * TILE_N, m0 = blockIdx.y * p.BN;
-  const int KS = p.NB * (256 / KSTEP);
-  const uint32_t x_stage_bytes = (uint32_t)p.BN * KSTEP * 2;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < p.SX; ++i) {
+    for (int i = 0; i < SX; ++i) {
       mbar_init(b_xfull + 8 * i, 1);
       mbar_init(b_xempty + 8 * i, 1);
     }
-    for (int i = 0; i < p.SW; ++i) {
-      mbar_init(b_wfull + 8 * i, 1);
-      mbar_init(b_wempty + 8 * i, 8);
-    }
-    for (int i = 0; i < p.SA; ++i) {
+    for (int i = 0; i < SA; ++i) {
       mbar_init(b_afull + 8 * i, 8);
       mbar_init(b_aempty + 8 * i, 1);
     }
-    mbar_init(b_acc, 1);
+    for (int i = 0; i < SW; ++i) {
+      mbar_init(b_wfull + 8 * i, 1);
+      mbar_init(b_wempty + 8 * i, 8);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(b_accfull + 8 * i, 1);
+      mbar_init(b_accempty + 8 * i, NUM_EPI_WARPS);
+    }
+    mbar_init(b_drain, 1);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
-  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), p.tmem_cols);
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  const long long u_begin = range_start(p, blockIdx.x), u_end = range_start(p, (long long)blockIdx.x + 1);
+
   auto fail = [&]() {
     *abort_flag = 1;
     atomicOr(&g_gemm_error, ERR_TIMEOUT);
   };
+  auto wait = [&](uint32_t bar, uint32_t parity) {
+    return mbar_wait_bounded(bar, parity, abort_flag, WAIT_LIMIT_NS);
+  };
 
   if (warp == 0) {
     if (lane == 0) {
-      // ------------------------------------------------------ TMA producer --
+      // ---------------------------------------------------------- TMA producer --
       tma_prefetch_desc(&tmX);
       tma_prefetch_desc(&tmW0);
       if (SWIGLU) tma_prefetch_desc(&tmW1);
-      int issued_x = 0, issued_w = 0;
-      for (int ks = 0; ks < KS; ++ks) {
-        if ((ks & 3) == 0) {
-          const int kb = ks >> 2, s = kb % p.SW;
-          if (!mbar_wait_bounded(b_wempty + 8 * s, ((kb / p.SW) & 1) ^ 1, abort_flag, WAIT_LIMIT_NS)) {
-            fail();
+      Ring<SX> rx;
+      Ring<SW> rw;
+      long long nx = 0, nw = 0;
+      bool ok = true;
+      UnitIter it{u_begin, u_end, p.KS};
+      while (ok && it.next()) {
+        const int nt = it.tile / p.m_tiles;
+        const int n0 = nt * TILE_N, m0 = (it.tile - nt * p.m_tiles) * p.BN;
+        for (int k = it.k0; k < it.k1; ++k) {
+          if (k == it.k0 || (k & 3) == 0) {
+            if (!wait(b_wempty + 8 * rw.s, rw.ph ^ 1u)) {
+              ok = false;
+              break;
+            }
+            const uint32_t bar = b_wfull + 8 * rw.s;
+            mbar_arrive_expect_tx(bar, W_STAGE_BYTES * NMAT);
+            tma_load_3d(sw + (uint32_t)(rw.s * NMAT) * W_STAGE_BYTES, &tmW0, bar, 0, k >> 2, n0);
+            if (SWIGLU) tma_load_3d(sw + (uint32_t)(rw.s * NMAT + 1) * W_STAGE_BYTES, &tmW1, bar, 0, k >> 2, n0);
+            rw.next();
+            ++nw;
+          }
+          if (!wait(b_xempty + 8 * rx.s, rx.ph ^ 1u)) {
+            ok = false;
             break;
           }
-          mbar_arrive_expect_tx(b_wfull + 8 * s, W_STAGE_BYTES * NMAT);
-          tma_load_3d(sw + (uint32_t)(s * NMAT) * W_STAGE_BYTES, &tmW0, b_wfull + 8 * s, 0, kb, n0);
-          if (SWIGLU)
-            tma_load_3d(sw + (uint32_t)(s * NMAT + 1) * W_STAGE_BYTES, &tmW1, b_wfull + 8 * s, 0, kb, n0);
-          issued_w = kb + 1;
+          mbar_arrive_expect_tx(b_xfull + 8 * rx.s, p.x_stage_bytes);
+          tma_load_2d(sx + (uint32_t)rx.s * p.x_stage_bytes, &tmX, b_xfull + 8 * rx.s, k * KSTEP, m0);
+          rx.next();
+          ++nx;
         }
-        const int s = ks % p.SX;
-        if (!mbar_wait_bounded(b_xempty + 8 * s, ((ks / p.SX) & 1) ^ 1, abort_flag, WAIT_LIMIT_NS)) {
-          fail();
-          break;
-        }
-        mbar_arrive_expect_tx(b_xfull + 8 * s, x_stage_bytes);
-        tma_load_2d(sx + (uint32_t)s * x_stage_bytes, &tmX, b_xfull + 8 * s, ks * KSTEP, m0);
-        issued_x = ks + 1;
       }
+      if (!ok) fail();
       // Every copy this thread issued must have landed before the CTA exits.
-      for (int i = issued_x - p.SX; i < issued_x; ++i)
-        if (i >= 0) mbar_wait_bounded(b_xfull + 8 * (i % p.SX), (i / p.SX) & 1, nullptr, WAIT_LIMIT_NS);
-      for (int i = issued_w - p.SW; i < issued_w; ++i)
-        if (i >= 0) mbar_wait_bounded(b_wfull + 8 * (i % p.SW), (i / p.SW) & 1, nullptr, WAIT_LIMIT_NS);
+      for (long long i = nx > SX ? nx - SX : 0; i < nx; ++i)
+        mbar_wait_bounded(b_xfull + 8 * (int)(i % SX), (uint32_t)((i / SX) & 1), nullptr, WAIT_LIMIT_NS);
+      for (long long i = nw > SW ? nw - SW : 0; i < nw; ++i)
+        mbar_wait_bounded(b_wfull + 8 * (int)(i % SW), (uint32_t)((i / SW) & 1), nullptr, WAIT_LIMIT_NS);
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      // ------------------------------------------------------- MMA issuer --
+      // ------------------------------------------------------------ MMA issuer --
       const uint32_t idesc = umma_idesc_f16(TILE_N, p.BN);
-      for (int ks = 0; ks < KS; ++ks) {
-        const int s_a = ks % p.SA, s_x = ks % p.SX;
-        if (!mbar_wait_bounded(b_afull + 8 * s_a, (ks / p.SA) & 1, abort_flag, WAIT_LIMIT_NS) ||
-            !mbar_wait_bounded(b_xfull + 8 * s_x, (ks / p.SX) & 1, abort_flag, WAIT_LIMIT_NS)) {
-          fail();
+      Ring<SA> ra;
+      Ring<SX> rx;
+      Ring<2> racc;
+      bool ok = true;
+      UnitIter it{u_begin, u_end, p.KS};
+      while (ok && it.next()) {
+        if (!wait(b_accempty + 8 * racc.s, racc.ph ^ 1u)) {
+          ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t a0 = sa + (uint32_t)(s_a * NMAT) * A_STAGE_BYTES;
-        const uint32_t b0 = sx + (uint32_t)s_x * x_stage_bytes;
+        const uint32_t d = tmem + (uint32_t)racc.s * ACC_COLS;
+        for (int k = it.k0; k < it.k1; ++k) {
+          if (!wait(b_xfull + 8 * rx.s, rx.ph) || !wait(b_afull + 8 * ra.s, ra.ph)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = sa + (uint32_t)(ra.s * NMAT) * A_STAGE_BYTES;
+          const uint32_t b0 = sx + (uint32_t)rx.s * p.x_stage_bytes;
 #pragma unroll
-        for (int kk = 0; kk < KSTEP / 16; ++kk) {
-          const uint64_t bd = umma_desc_sw128(b0 + 32 * kk);
-          const uint32_t acc = (ks | kk) != 0;
-          umma_f16(tmem, umma_desc_sw128(a0 + 32 * kk), bd, idesc, acc);
-          if (SWIGLU) umma_f16(tmem + (p.tmem_cols >> 1), umma_desc_sw128(a0 + A_STAGE_BYTES + 32 * kk), bd, idesc, acc);
+          for (int kk = 0; kk < KSTEP / 16; ++kk) {
+            const uint64_t bd = umma_desc_sw128(b0 + 32 * kk);
+            const uint32_t acc = (k > it.k0 || kk > 0) ? 1u : 0u;
+            umma_f16(d, umma_desc_sw128(a0 + 32 * kk), bd, idesc, acc);
+            if (SWIGLU) umma_f16(d + 128, umma_desc_sw128(a0 + A_STAGE_BYTES + 32 * kk), bd, idesc, acc);
+          }
+          umma_commit(b_aempty + 8 * ra.s);
+          umma_commit(b_xempty + 8 * rx.s);
+          ra.next();
+          rx.next();
         }
-        umma_commit(b_aempty + 8 * s_a);
-        umma_commit(b_xempty + 8 * s_x);
+        if (!ok) break;
+        umma_commit(b_accfull + 8 * racc.s);
+        racc.next();
       }
-      umma_commit(b_acc);  // also tracks every MMA issued before an abort
-      mbar_wait_bounded(b_acc, 0, nullptr, WAIT_LIMIT_NS);
+      if (!ok) fail();
+      umma_commit(b_drain);  // tracks every MMA issued, also after an abort
+      mbar_wait_bounded(b_drain, 0, nullptr, WAIT_LIMIT_NS);
     }
-  } else {
-    // ------------------------------------------------- dequant + epilogue --
-    // Warps 2..9: warp w handles TMEM lane quarter q = w & 3 (rows 32q..32q+31)
-    // and nibble side hs = (w - 2) >> 2: hs = 0 makes sub-block 2c (low
-    // nibbles, k 0..31 of the step), hs = 1 sub-block 2c+1 (high nibbles,
-    // k 32..63).
+  } else if (warp < EPI_WARP0) {
+    // --------------------------------------------------------------- dequant --
+    // Warp w handles TMEM lane quarter q = w & 3 (rows 32q..32q+31) and nibble
+    // side hs = (w - 2) >> 2: hs = 0 makes sub-block 2c (low nibbles, k 0..31
+    // of the step), hs = 1 sub-block 2c+1 (high nibbles, k 32..63).
     const int q = warp & 3;
     const int hs = (warp - 2) >> 2;
-    const int r = 32 * q + lane;  // weight row within the tile
+    const int r = 32 * q + lane;
+    const uint32_t mask = hs ? 0x00F000F0u : 0x000F000Fu;
+    Ring<SA> ra;
+    Ring<SW> rw;
     bool ok = true;
-    for (int ks = 0; ks < KS && ok; ++ks) {
-      const int kb = ks >> 2, c = ks & 3, s_w = kb % p.SW, s_a = ks % p.SA;
-      // Waits are made warp-uniform so that a timeout leaves the warp converged.
-      if (c == 0) ok = __all_sync(0xffffffffu, mbar_wait_bounded(b_wfull + 8 * s_w, (kb / p.SW) & 1, abort_flag, WAIT_LIMIT_NS));
-      if (ok) ok = __all_sync(0xffffffffu, mbar_wait_bounded(b_aempty + 8 * s_a, ((ks / p.SA) & 1) ^ 1, abort_flag, WAIT_LIMIT_NS));
-      if (!ok) break;
+    UnitIter it{u_begin, u_end, p.KS};
+    while (ok && it.next()) {
+      for (int k = it.k0; k < it.k1; ++k) {
+        const int c = k & 3;
+        // Waits are made warp-uniform so that a timeout leaves the warp converged.
+        if (k == it.k0 || c == 0) ok = __all_sync(0xffffffffu, wait(b_wfull + 8 * rw.s, rw.ph));
+        if (ok) ok = __all_sync(0xffffffffu, wait(b_aempty + 8 * ra.s, ra.ph ^ 1u));
+        if (!ok) break;
 #pragma unroll
-      for (int mat = 0; mat < NMAT; ++mat) {
-        const uint8_t* raw = smem + p.off_w + (size_t)(s_w * NMAT + mat) * W_STAGE_BYTES + (size_t)r * BLOCK_BYTES;
-        const uint4 hd = *reinterpret_cast<const uint4*>(raw);
-        const uint4 q0 = *reinterpret_cast<const uint4*>(raw + 16 + 32 * c);
-        const uint4 q1 = *reinterpret_cast<const uint4*>(raw + 32 + 32 * c);
-        uint32_t sc, m;
-        q4k_scale_min(hd.y, hd.z, hd.w, 2 * c + hs, sc, m);
-        // p = sc*q exactly in fp16 from the offset code h (1024+q or 1024+16q):
-        //   p = h*sc - 1024*sc  or  p = h*(sc/16) - 64*sc   (one rounding of an
-        //   exact integer <= 945).  Then w = fma(d, p, -dmin*m) in fp32 is the
-        //   exact value rounded once, i.e. the fp32 dequant, rounded to fp16.
-        const __half sch = __uint2half_rn(sc);
-        const __half2 scv = __half2half2(hs ? __hmul(sch, __float2half(0.0625f)) : sch);
-        const __half2 offv = __half2half2(__hmul(sch, __float2half(hs ? -64.f : -1024.f)));
-        const uint32_t scv_u = *reinterpret_cast<const uint32_t*>(&scv);
-        const uint32_t offv_u = *reinterpret_cast<const uint32_t*>(&offv);
-        const unsigned short d16 = (unsigned short)(hd.x & 0xffffu);
-        const float nt = -__fmul_rn(half_hi_to_float(hd.x), (float)m);
-        const uint32_t mask = hs ? 0x00F000F0u : 0x000F000Fu;
-        const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-        uint8_t* arow = smem + p.off_a + (size_t)(s_a * NMAT + mat) * A_STAGE_BYTES + (size_t)r * 128;
+        for (int mat = 0; mat < NMAT; ++mat) {
+          const uint8_t* raw = smem + p.off_w + (size_t)(rw.s * NMAT + mat) * W_STAGE_BYTES + (size_t)r * BLOCK_BYTES;
+          const uint4 hd = *reinterpret_cast<const uint4*>(raw);
+          const uint4 q0 = *reinterpret_cast<const uint4*>(raw + 16 + 32 * c);
+          const uint4 q1 = *reinterpret_cast<const uint4*>(raw + 32 + 32 * c);
+          uint32_t sc, m;
+          q4k_scale_min(hd.y, hd.z, hd.w, 2 * c + hs, sc, m);
+          // p = sc*q exactly in fp16 from the offset code h (1024+q or 1024+16q):
+          //   p = h*sc - 1024*sc  or  p = h*(sc/16) - 64*sc   (one rounding of an
+          //   exact integer <= 945).  Then w = fma(d, p, -dmin*m) in fp32 is the
+          //   exact value rounded once, i.e. the fp32 dequant, rounded to fp16.
+          const __half sch = __uint2half_rn(sc);
+          const __half2 scv = __half2half2(hs ? __hmul(sch, __float2half(0.0625f)) : sch);
+          const __half2 offv = __half2half2(__hmul(sch, __float2half(hs ? -64.f : -1024.f)));
+          const uint32_t scv_u = *reinterpret_cast<const uint32_t*>(&scv);
+          const uint32_t offv_u = *reinterpret_cast<const uint32_t*>(&offv);
+          const unsigned short d16 = (unsigned short)(hd.x & 0xffffu);
+          const float nt = -__fmul_rn(half_hi_to_float(hd.x), (float)m);
+          const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+          uint8_t* arow = smem + p.off_a + (size_t)(ra.s * NMAT + mat) * A_STAGE_BYTES + (size_t)r * 128;
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          // output chunk j8 = 4*hs + jj holds k = 8*j8..8*j8+7: code bytes 8*jj..8*jj+7
-          uint32_t pk[4];
+          for (int jj = 0; jj < 4; ++jj) {
+            // output chunk j8 = 4*hs + jj holds k = 8*j8..8*j8+7: code bytes 8*jj..8*jj+7
+            uint32_t pk[4];
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const uint32_t w = qw[2 * jj + e];
-            uint32_t wp;
-            asm("prmt.b32 %0, %1, 0, 0x3120;" : "=r"(wp) : "r"(w));  // bytes b0 b2 b1 b3
-            pk[2 * e] = dq_pair(lop3_and_or(wp, mask, 0x64006400u), scv_u, offv_u, d16, nt);       // k, k+1
-            pk[2 * e + 1] = dq_pair(lop3_and_or(wp >> 8, mask, 0x64006400u), scv_u, offv_u, d16, nt);  // k+2, k+3
+            for (int e = 0; e < 2; ++e) {
+              const uint32_t w = qw[2 * jj + e];
+              uint32_t wp;
+              asm("prmt.b32 %0, %1, 0, 0x3120;" : "=r"(wp) : "r"(w));  // bytes b0 b2 b1 b3
+              pk[2 * e] = dq_pair(lop3_and_or(wp, mask, 0x64006400u), scv_u, offv_u, d16, nt);       // k, k+1
+              pk[2 * e + 1] = dq_pair(lop3_and_or(wp >> 8, mask, 0x64006400u), scv_u, offv_u, d16, nt);  // k+2, k+3
+            }
+            const int j8 = 4 * hs + jj;
+            *reinterpret_cast<uint4*>(arow + ((j8 ^ (r & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
           }
-          const int j8 = 4 * hs + jj;
-          *reinterpret_cast<uint4*>(arow + ((j8 ^ (r & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(b_afull + 8 * ra.s);
+        ra.next();
+        if (k == it.k1 - 1 || c == 3) {
+          if (lane == 0) mbar_arrive(b_wempty + 8 * rw.s);
+          rw.next();
         }
       }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(b_afull + 8 * s_a);
-        if (c == 3) mbar_arrive(b_wempty + 8 * s_w);
-      }
     }
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait_bounded(b_acc, 0, abort_flag, WAIT_LIMIT_NS));
-    if (!ok) {
-      if (lane == 0) fail();
-    } else {
+    if (!ok && lane == 0) fail();
+  } else {
+    // -------------------------------------------------------------- epilogue --
+    // Warp w reads TMEM lane quarter q = w & 3: rows 32q..32q+31 of the tile.
+    const int q = warp & 3;
+    const int r = 32 * q + lane;
+    Ring<2> racc;
+    bool ok = true;
+    UnitIter it{u_begin, u_end, p.KS};
+    while (ok && it.next()) {
+      ok = __all_sync(0xffffffffu, wait(b_accfull + 8 * racc.s, racc.ph));
+      if (!ok) break;
       tc_fence_after();
-      const int n = n0 + r;
-      const uint32_t lane_addr = tmem + ((uint32_t)(32 * q) << 16);
-      // the two warps of a lane quarter split the token columns in 32-wide chunks
-      for (int cc = 32 * hs; cc < p.BN; cc += 64) {
-        uint32_t v[32];
-        tmem_ld32(lane_addr + cc, v);
-        if (SWIGLU) {
-          uint32_t u[32];
-          tmem_ld32(lane_addr + (p.tmem_cols >> 1) + cc, u);
-          if (n < p.N) {
-            __half* y = reinterpret_cast<__half*>(p.y);
+      const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)racc.s * ACC_COLS;
+      const int nt = it.tile / p.m_tiles;
+      const int n = nt * TILE_N + r, m0 = (it.tile - nt * p.m_tiles) * p.BN;
+      const bool writer = it.k0 > 0;                  // later part of a cut tile
+      const bool fixer = !writer && it.k1 < p.KS;      // first part of a cut tile
+      constexpr int MAT_COLS = SWIGLU ? 128 : 0;       // TMEM column offset of the second matrix
+      if (writer) {
+        // Leave the fp32 partial in this CTA's slot ([column][row], coalesced
+        // over rows), then count this warp in the slot's flag.
+        float* slot = p.partial + (size_t)blockIdx.x * SLOT_FLOATS;
+        for (int mat = 0; mat < NMAT; ++mat) {
+          for (int cc = 0; cc < p.BN; cc += 32) {
+            uint32_t v[32];
+            tmem_ld32(tl + mat * MAT_COLS + cc, v);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const int m = m0 + cc + j;
-              if (m < p.M && cc + j < p.BN) {
-                const float g = __uint_as_float(v[j]), uu = __uint_as_float(u[j]);
-                y[(size_t)m * p.N + n] = __float2half_rn(g / (1.0f + expf(-g)) * uu);
+            for (int j = 0; j < 32; ++j) __stcg(slot + (size_t)(mat * MAT_COLS + cc + j) * TILE_N + r, __uint_as_float(v[j]));
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(b_accempty + 8 * racc.s);
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) atom_add_release_gpu(p.flags + blockIdx.x, 1u);
+      } else {
+        // Contributors to a cut tile: the CTAs after this one whose ranges
+        // start inside it, summed in CTA order.
+        int j_end = blockIdx.x + 1;
+        if (fixer) {
+          const long long tile_end = (long long)(it.tile + 1) * p.KS;
+          while (j_end < (int)gridDim.x && range_start(p, j_end) < tile_end) ++j_end;
+          for (int j = blockIdx.x + 1; j < j_end && ok; ++j) {
+            bool ready = false;
+            const uint64_t t0 = globaltimer_ns();
+            for (uint32_t it2 = 0;; ++it2) {
+              if (ld_acquire_gpu(p.flags + j) >= (uint32_t)NUM_EPI_WARPS) {
+                ready = true;
+                break;
+              }
+              if ((it2 & 63u) == 63u && (*abort_flag || globaltimer_ns() - t0 > WAIT_LIMIT_NS)) break;
+            }
+            ok = __all_sync(0xffffffffu, ready);
+          }
+          if (!ok) break;
+        }
+        for (int cc = 0; cc < p.BN; cc += 32) {
+          uint32_t v[32];
+          tmem_ld32(tl + cc, v);
+          float a[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) a[j] = __uint_as_float(v[j]);
+          for (int jc = blockIdx.x + 1; jc < j_end; ++jc) {
+            const float* slot = p.partial + (size_t)jc * SLOT_FLOATS + (size_t)cc * TILE_N + r;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) a[j] += __ldcg(slot + (size_t)j * TILE_N);
+          }
+          if (SWIGLU) {
+            tmem_ld32(tl + MAT_COLS + cc, v);
+            float u[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) u[j] = __uint_as_float(v[j]);
+            for (int jc = blockIdx.x + 1; jc < j_end; ++jc) {
+              const float* slot = p.partial + (size_t)jc * SLOT_FLOATS + (size_t)(MAT_COLS + cc) * TILE_N + r;
+#pragma unroll
+              for (int j = 0; j < 32; ++j) u[j] += __ldcg(slot + (size_t)j * TILE_N);
+            }
+            if (n < p.N) {
+              __half* y = reinterpret_cast<__half*>(p.y);
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                const int m = m0 + cc + j;
+                if (cc + j < p.BN && m < p.M) y[(size_t)m * p.N + n] = __float2half_rn(a[j] / (1.0f + expf(-a[j])) * u[j]);
+              }
+            }
+          } else if (n < p.N) {
+            if (p.out_f16) {
+              __half* y = reinterpret_cast<__half*>(p.y);
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                const int m = m0 + cc + j;
+                if (cc + j < p.BN && m < p.M) y[(size_t)m * p.N + n] = __float2half_rn(a[j]);
+              }
+            } else {
+              float* y = reinterpret_cast<float*>(p.y);
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                const int m = m0 + cc + j;
+                if (cc + j < p.BN && m < p.M) y[(size_t)m * p.N + n] = a[j];
               }
             }
           }
-        } else if (n < p.N) {
-          if (p.out_f16) {
-            __half* y = reinterpret_cast<__half*>(p.y);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const int m = m0 + cc + j;
-              if (m < p.M && cc + j < p.BN) y[(size_t)m * p.N + n] = __float2half_rn(__uint_as_float(v[j]));
-            }
-          } else {
-            float* y = reinterpret_cast<float*>(p.y);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const int m = m0 + cc + j;
-              if (m < p.M && cc + j < p.BN) y[(size_t)m * p.N + n] = __uint_as_float(v[j]);
-            }
-          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(b_accempty + 8 * racc.s);
+          // The last of the four epilogue warps to finish returns the
+          // contributors' flags to zero for the next call.
+          for (int jc = blockIdx.x + 1; jc < j_end; ++jc)
+            if (atom_add_acqrel_gpu(p.flags + jc, 1u) == 2 * NUM_EPI_WARPS - 1) p.flags[jc] = 0;
         }
       }
+      racc.next();
     }
+    if (!ok && lane == 0) fail();
   }
 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, p.tmem_cols);
+  if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
 }
 
 // ---------------------------------------------------------------- host --
@@ -350,70 +545,116 @@ cudaError_t make_maps(const void* w0, const void* w1, const void* x, int64_t M, 
   return cudaSuccess;
 }
 
+// Tuning knobs read once from the environment:
+//   JLLM_GEMM_BN     tokens per tile (multiple of 16, at most the kernel's cap)
+//   JLLM_GEMM_SPLIT  0 keeps whole tiles even when a workspace is given
+struct GemmKnobs {
+  int bn = 0;
+  int split = 1;
+};
+const GemmKnobs& gemm_knobs() {
+  static GemmKnobs k = [] {
+    GemmKnobs v;
+    if (const char* e = getenv("JLLM_GEMM_BN")) v.bn = atoi(e);
+    if (const char* e = getenv("JLLM_GEMM_SPLIT")) v.split = atoi(e);
+    return v;
+  }();
+  return k;
+}
+
 template <bool SWIGLU>
-cudaError_t launch_tc(const CUtensorMap& mx, const CUtensorMap& mw0, const CUtensorMap& mw1, GemmParams p,
-                      int64_t N, cudaStream_t s, size_t smem) {
+cudaError_t launch_tc(const CUtensorMap& mx, const CUtensorMap& mw0, const CUtensorMap& mw1, const GemmParams& p,
+                      int grid, bool cooperative, size_t smem, cudaStream_t s) {
   auto kern = q4k_gemm_tc_kernel<SWIGLU>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)((N + TILE_N - 1) / TILE_N), (unsigned)((p.M + p.BN - 1) / p.BN));
-  kern<<<grid, 320, smem, s>>>(mx, mw0, mw1, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = cooperative ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, mx, mw0, mw1, p);
 }
 
 }  // namespace
 
+size_t gemm_workspace_bytes() {
+  const DevInfo& dev = device_info();
+  if (dev.err != cudaSuccess || dev.sm_count <= 0) return 0;
+  const size_t bytes = (size_t)dev.sm_count * SLOT_FLOATS * sizeof(float) + (size_t)dev.sm_count * sizeof(uint32_t);
+  return (bytes + 255) & ~(size_t)255;
+}
+
 cudaError_t launch_gemm_tc(const void* w0, const void* w1, const void* x, void* y, bool y_f16, int64_t M,
-                           int64_t N, int64_t K, cudaStream_t s) {
+                           int64_t N, int64_t K, void* ws, size_t ws_bytes, cudaStream_t s) {
   const DevInfo& dev = device_info();
   const bool swiglu = w1 != nullptr;
   const int nmat = swiglu ? 2 : 1;
   if (M > INT32_MAX / 2 || N > INT32_MAX / 2 || K / QK > INT32_MAX / 8) return cudaErrorInvalidValue;
-  // Tokens per CTA: the whole of M up to 256 (rounded up to 16), else 256
-  // (128 when the SwiGLU epilogue needs two accumulators).  Stage counts:
-  // raw-W and dequantised-A rings first, the rest of shared memory for X.
-  // JLLM_GEMM_BN / _SA / _SW override (tuning).
-  static const int env_bn = getenv("JLLM_GEMM_BN") ? atoi(getenv("JLLM_GEMM_BN")) : 0;
-  static const int env_sa = getenv("JLLM_GEMM_SA") ? atoi(getenv("JLLM_GEMM_SA")) : 0;
-  static const int env_sw = getenv("JLLM_GEMM_SW") ? atoi(getenv("JLLM_GEMM_SW")) : 0;
-  int bn_cap = swiglu ? 128 : 256;
-  if (env_bn >= 16 && env_bn <= bn_cap && env_bn % 16 == 0) bn_cap = env_bn;
+  const GemmKnobs& kn = gemm_knobs();
+  // Tokens per tile: the whole of M up to the cap (rounded up to 16), else
+  // the cap: 256, or 128 when the SwiGLU epilogue needs two accumulators.
+  int bn_cap = swiglu ? Cfg<true>::BN_MAX : Cfg<false>::BN_MAX;
+  if (kn.bn >= 16 && kn.bn <= bn_cap && kn.bn % 16 == 0) bn_cap = kn.bn;
   int BN = (int)((M + 15) / 16 * 16);
   if (BN > bn_cap) BN = bn_cap;
-  uint32_t cols = 32;
-  while (cols < (uint32_t)(BN * nmat)) cols <<= 1;
 
-  GemmParams p;
+  GemmParams p = {};
   p.y = y;
   p.M = (int)M;
   p.N = (int)N;
   p.NB = (int)(K / QK);
   p.BN = BN;
-  p.tmem_cols = cols;
+  p.m_tiles = (int)((M + BN - 1) / BN);
+  p.KS = 4 * p.NB;
   p.out_f16 = (y_f16 || swiglu) ? 1 : 0;
-  p.SW = env_sw > 0 ? env_sw : 3;
-  p.SA = env_sa > 0 ? env_sa : 3;
-  const size_t x_stage = (size_t)BN * KSTEP * 2;
-  const size_t budget = dev.smem_optin - 1024 /*alignment*/ - 512 /*barriers*/;
-  size_t fixed = (size_t)p.SW * W_STAGE_BYTES * nmat + (size_t)p.SA * A_STAGE_BYTES * nmat;
-  while (fixed + 2 * x_stage > budget && (p.SW > 2 || p.SA > 2)) {
-    if (p.SW >= p.SA && p.SW > 2) --p.SW; else --p.SA;
-    fixed = (size_t)p.SW * W_STAGE_BYTES * nmat + (size_t)p.SA * A_STAGE_BYTES * nmat;
+  const long long tiles = (long long)p.m_tiles * ((N + TILE_N - 1) / TILE_N);
+  const long long units = tiles * p.KS;
+  if (units > (1ll << 53)) return cudaErrorInvalidValue;
+  const int sms = dev.sm_count;
+
+  // Stream-K when the tiles do not fill the SMs evenly and a workspace is
+  // given; each CTA then takes at least 8 K steps.
+  const bool split = kn.split != 0 && ws != nullptr && ws_bytes >= gemm_workspace_bytes() && tiles % sms != 0;
+  int grid;
+  if (split) {
+    long long g = units / 8;
+    if (g > sms) g = sms;
+    if (g < 1) g = 1;
+    grid = (int)g;
+    p.grain = 1;
+    p.grains = units;
+    p.partial = reinterpret_cast<float*>(ws);
+    p.flags = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(ws) + (size_t)sms * SLOT_FLOATS * sizeof(float));
+  } else {
+    grid = (int)(tiles < sms ? tiles : sms);
+    p.grain = p.KS;
+    p.grains = tiles;
   }
-  if (fixed + 2 * x_stage > budget) return cudaErrorInvalidValue;
-  size_t sxn = (budget - fixed) / x_stage;
-  if (sxn > 8) sxn = 8;
-  p.SX = (int)sxn;
+
+  // Shared memory: X ring, dequantised-A ring, raw-W ring, barriers.
+  const int SX = swiglu ? Cfg<true>::SX : Cfg<false>::SX;
+  const int SA = swiglu ? Cfg<true>::SA : Cfg<false>::SA;
+  const int SW = swiglu ? Cfg<true>::SW : Cfg<false>::SW;
+  const int nbars = swiglu ? Cfg<true>::NBARS : Cfg<false>::NBARS;
+  p.x_stage_bytes = (uint32_t)BN * KSTEP * 2;
   p.off_x = 0;
-  p.off_a = (uint32_t)(p.SX * x_stage);
-  p.off_w = p.off_a + (uint32_t)(p.SA * A_STAGE_BYTES * nmat);
-  p.off_bar = p.off_w + (uint32_t)(p.SW * W_STAGE_BYTES * nmat);
-  const size_t smem = 1024 + p.off_bar + 8 * (2 * (p.SX + p.SW + p.SA) + 1) + 16;
+  p.off_a = (uint32_t)SX * p.x_stage_bytes;
+  p.off_w = p.off_a + (uint32_t)(SA * nmat * A_STAGE_BYTES);
+  p.off_bar = p.off_w + (uint32_t)(SW * nmat * W_STAGE_BYTES);
+  const size_t smem = 1024 + p.off_bar + 8 * nbars + 16;
+  if (smem > dev.smem_optin) return cudaErrorInvalidValue;
 
   CUtensorMap mx, mw0, mw1;
   cudaError_t e = make_maps(w0, w1, x, M, N, K, BN, &mx, &mw0, &mw1);
   if (e != cudaSuccess) return e;
-  return swiglu ? launch_tc<true>(mx, mw0, mw1, p, N, s, smem) : launch_tc<false>(mx, mw0, mw1, p, N, s, smem);
+  return swiglu ? launch_tc<true>(mx, mw0, mw1, p, grid, split, smem, s)
+                : launch_tc<false>(mx, mw0, mw1, p, grid, split, smem, s);
 }
 
 cudaError_t read_clear_gemm_error(uint32_t* bits, cudaStream_t s) {

@@ -560,7 +560,7 @@ struct Knobs {
   int ctas_per_sm = 1;
   int R = 0, W = 0, KS = 0;
   int trigger = 1;
-  int stream = 0;             // JLLM_GEMV_STREAM=0 disables the streaming kernel
+  int stream = 0;             // JLLM_GEMV_STREAM=1 selects the streaming kernel (off by default)
   int sC = 0, sR = 0, sKS = 0;  // JLLM_GEMV_SCFG="C,R" forces the consumer warps and rows of the streaming kernel
   int smem_kb = 100;          // JLLM_GEMV_SMEM_KB: shared-memory budget of a streaming CTA
   int pre_pct = 100;          // JLLM_GEMV_PRE: % of a CTA's warps whose rows are fetched before the wait

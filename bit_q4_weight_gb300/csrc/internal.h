@@ -28,10 +28,15 @@ cudaError_t launch_gemv(const void* w0, const void* w1, const void* x, void* y, 
                         cudaStream_t s);
 
 // TMA + tcgen05 GEMM for any M >= 1.  w1 != nullptr selects the SwiGLU
-// epilogue (y = fp16 h).  Returns cudaErrorInvalidValue for unsupported
-// shapes.
+// epilogue (y = fp16 h).  ws (nullptr allowed) of at least
+// gemm_workspace_bytes() zero-initialised bytes enables the stream-K split.
+// Returns cudaErrorInvalidValue for unsupported shapes.
 cudaError_t launch_gemm_tc(const void* w0, const void* w1, const void* x, void* y, bool y_f16, int64_t M,
-                           int64_t N, int64_t K, cudaStream_t s);
+                           int64_t N, int64_t K, void* ws, size_t ws_bytes, cudaStream_t s);
+
+// Workspace of the stream-K split on the current device: one 128 KiB fp32
+// partial slot and one flag word per SM (0 when the device is unusable).
+size_t gemm_workspace_bytes();
 
 // Read and clear the device error word of the tcgen05 kernels (after
 // synchronising the stream) and of the GEMV kernels.

@@ -64,7 +64,7 @@ typedef enum {
                                      size beyond the kernels' index range      */
   JLLM_ERR_MISALIGNED = 3,        /* a pointer not 16-byte aligned             */
   JLLM_ERR_UNSUPPORTED_DTYPE = 4, /* output dtype not allowed for this call    */
-  JLLM_ERR_WORKSPACE = 5,         /* workspace missing, too small or misaligned */
+  JLLM_ERR_WORKSPACE = 5,         /* workspace too small or misaligned */
   JLLM_ERR_CUDA = 6,              /* a CUDA runtime/driver call failed         */
   JLLM_ERR_DEVICE_TIMEOUT = 7,    /* a kernel-side bounded wait ran out        */
   JLLM_ERR_NO_DEVICE = 8          /* the current device is not sm_103          */
@@ -91,8 +91,8 @@ jllm_status jllm_q4k_dequant(const void* w_q4k, void* out, jllm_dtype out_dt, in
  *   w_q4k : W, [N][K/256] blocks
  *   x     : [K] fp16
  *   y     : [N] fp32
- *   ws, ws_bytes : workspace, at least jllm_q4k_workspace_bytes(1, N, K)
- *           bytes (may be NULL/0 when that is 0), 16-byte aligned
+ *   ws, ws_bytes : unused by the GEMV (jllm_q4k_workspace_bytes(1, N, K)
+ *           is 0); may be NULL/0
  * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED, WORKSPACE, CUDA.
  */
 jllm_status jllm_q4k_gemv(const void* w_q4k, const void* x, float* y, int64_t N, int64_t K,
@@ -105,10 +105,13 @@ jllm_status jllm_q4k_gemv(const void* w_q4k, const void* x, float* y, int64_t N,
  *   w_q4k : W, [N][K/256] blocks
  *   x     : [M][K] fp16
  *   y     : [M][N], fp32 or fp16 (y_dt)
- *   ws, ws_bytes : workspace, at least jllm_q4k_workspace_bytes(M, N, K)
+ *   ws, ws_bytes : optional workspace (see jllm_q4k_workspace_bytes)
  * M <= jllm_q4k_gemv_max_m() runs the GEMV kernel (gemm(M=1) == gemv);
  * larger M runs the TMA + tcgen05 kernel (fp16 dequantised W, fp32
- * accumulation in tensor memory).
+ * accumulation in tensor memory).  With a workspace the tcgen05 kernel
+ * shares the K steps of the last wave of tiles evenly among the SMs
+ * (stream-K); the cut tiles' fp32 partials are added in a fixed order, so
+ * results are deterministic for a given device.
  * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED, UNSUPPORTED_DTYPE,
  *         WORKSPACE, CUDA.
  */
@@ -122,7 +125,7 @@ jllm_status jllm_q4k_gemm(const void* w_q4k, const void* x, void* y, jllm_dtype 
  *   w_gate, w_up : two Q4_K matrices, each [N][K/256] blocks
  *   x     : [M][K] fp16
  *   h     : [M][N] fp16
- *   ws, ws_bytes : at least jllm_q4k_workspace_bytes(M, N, K) bytes
+ *   ws, ws_bytes : optional workspace, as for jllm_q4k_gemm
  * g and u are each accurate to the matmul bound above; h is silu(g)*u
  * evaluated in fp32 and rounded to fp16.
  * Errors: as jllm_q4k_gemm.
@@ -131,7 +134,16 @@ jllm_status jllm_q4k_ffn_swiglu(const void* w_gate, const void* w_up, const void
                                 int64_t M, int64_t N, int64_t K, void* ws, size_t ws_bytes,
                                 jllm_stream_t stream);
 
-/* Workspace bytes that gemv/gemm/ffn_swiglu need for this shape (0 = none). */
+/*
+ * Workspace bytes that gemm/ffn_swiglu can use for this shape on the current
+ * device (0 = the call takes none).  Passing ws = NULL is always allowed and
+ * only gives up the stream-K split.  A workspace that is given must be at
+ * least this large, 256-byte aligned, and zero-filled before its first use;
+ * every call that completes leaves it zero-filled where that matters, so it
+ * can be reused by later calls, one call at a time (calls on different
+ * streams need different workspaces).  After JLLM_ERR_DEVICE_TIMEOUT,
+ * zero-fill it again.  Owned by the caller.
+ */
 size_t jllm_q4k_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
 /* Largest M that jllm_q4k_gemm sends to the GEMV kernel. */
