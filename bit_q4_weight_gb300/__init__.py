@@ -40,6 +40,7 @@ EXPORTS = (
     "jllm_q4k_dequant",
     "jllm_q4k_gemv",
     "jllm_q4k_gemm",
+    "jllm_q4k_gemm_noalloc",
     "jllm_q4k_ffn_swiglu",
     "jllm_q4k_workspace_bytes",
     "jllm_q4k_gemv_max_m",
@@ -72,6 +73,8 @@ lib.jllm_q4k_gemv.argtypes = [_P, _P, _P, _I64, _I64, _P, _SZ, _P]
 lib.jllm_q4k_gemv.restype = _ST
 lib.jllm_q4k_gemm.argtypes = [_P, _P, _P, ctypes.c_int, _I64, _I64, _I64, _P, _SZ, _P]
 lib.jllm_q4k_gemm.restype = _ST
+lib.jllm_q4k_gemm_noalloc.argtypes = [_P, _P, _P, ctypes.c_int, _I64, _I64, _I64, _P]
+lib.jllm_q4k_gemm_noalloc.restype = _ST
 lib.jllm_q4k_ffn_swiglu.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P]
 lib.jllm_q4k_ffn_swiglu.restype = _ST
 lib.jllm_q4k_workspace_bytes.argtypes = [_I64, _I64, _I64]
@@ -224,6 +227,26 @@ def jllm_q4k_gemm(w, x, N: int, K: int, out_dtype=None, out=None, ws=None, strea
                           ws.data_ptr() if ws is not None else None, nbytes, _stream_ptr(stream)),
         "jllm_q4k_gemm",
     )
+    return out
+
+
+def jllm_q4k_gemm_noalloc(w, x, N: int, K: int, out_dtype=None, out=None, stream=None):
+    """As jllm_q4k_gemm, with the library's static device workspace (no allocation)."""
+    torch = _torch()
+    _need(w, torch.uint8, _w_shape(N, K), "w")
+    if x.dim() != 2:
+        raise ValueError("x must be [M, K]")
+    M = int(x.shape[0])
+    _need(x, torch.float16, (M, K), "x")
+    out_dtype = out_dtype or (out.dtype if out is not None else torch.float32)
+    if out_dtype not in (torch.float32, torch.float16):
+        raise TypeError("out_dtype must be torch.float32 or torch.float16")
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=w.device)
+    _need(out, out_dtype, (M, N), "out")
+    dt = JLLM_F16 if out_dtype == torch.float16 else JLLM_F32
+    _check(lib.jllm_q4k_gemm_noalloc(w.data_ptr(), x.data_ptr(), out.data_ptr(), dt, M, N, K, _stream_ptr(stream)),
+           "jllm_q4k_gemm_noalloc")
     return out
 
 

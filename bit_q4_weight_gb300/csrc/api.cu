@@ -153,6 +153,25 @@ jllm_status jllm_q4k_gemm(const void* w_q4k, const void* x, void* y, jllm_dtype 
   return from_cuda(jllm::launch_gemm_tc(w_q4k, nullptr, x, y, y_dt == JLLM_F16, M, N, K, ws, ws_bytes, s));
 }
 
+jllm_status jllm_q4k_gemm_noalloc(const void* w_q4k, const void* x, void* y, jllm_dtype y_dt, int64_t M,
+                                  int64_t N, int64_t K, jllm_stream_t stream) {
+  if (!w_q4k || !x || !y) return JLLM_ERR_INVALID_ARG;
+  jllm_status st = check_shape(M, N, K);
+  if (st != JLLM_OK) return st;
+  if (y_dt != JLLM_F32 && y_dt != JLLM_F16) return JLLM_ERR_UNSUPPORTED_DTYPE;
+  if (!aligned16(w_q4k) || !aligned16(x) || !aligned16(y)) return JLLM_ERR_MISALIGNED;
+  if ((st = check_device()) != JLLM_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (M <= gemv_max_m() && y_dt == JLLM_F32)
+    return from_cuda(jllm::launch_gemv(w_q4k, nullptr, x, y, N, K, s));
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+  cudaError_t e = jllm::gemm_static_workspace(&ws, &ws_bytes);
+  if (e != cudaSuccess) return JLLM_ERR_CUDA;
+  if (ws_bytes < jllm_q4k_workspace_bytes(M, N, K)) return JLLM_ERR_WORKSPACE;  // more SMs than it was sized for
+  return from_cuda(jllm::launch_gemm_tc(w_q4k, nullptr, x, y, y_dt == JLLM_F16, M, N, K, ws, ws_bytes, s));
+}
+
 jllm_status jllm_q4k_ffn_swiglu(const void* w_gate, const void* w_up, const void* x, void* h, int64_t M,
                                 int64_t N, int64_t K, void* ws, size_t ws_bytes, jllm_stream_t stream) {
   if (!w_gate || !w_up || !x || !h) return JLLM_ERR_INVALID_ARG;

@@ -581,7 +581,34 @@ cudaError_t launch_tc(const CUtensorMap& mx, const CUtensorMap& mw0, const CUten
   return cudaLaunchKernelEx(&cfg, kern, mx, mw0, mw1, p);
 }
 
+// Library-owned workspace of jllm_q4k_gemm_noalloc: zero at module load,
+// returned to zero by every call that completes.  Sized for up to
+// kStaticWsSMs SMs.
+constexpr int kStaticWsSMs = 160;
+constexpr size_t kStaticWsBytes =
+    ((size_t)kStaticWsSMs * SLOT_FLOATS * sizeof(float) + (size_t)kStaticWsSMs * sizeof(uint32_t) + 255) & ~(size_t)255;
+__device__ __align__(256) uint8_t g_static_ws[kStaticWsBytes];
+
+constexpr int kMaxDevices = 64;
+void* g_static_ws_ptr[kMaxDevices];
+cudaError_t g_static_ws_err[kMaxDevices];
+std::once_flag g_static_ws_once[kMaxDevices];
+
 }  // namespace
+
+cudaError_t gemm_static_workspace(void** ptr, size_t* bytes) {
+  int d = 0;
+  cudaError_t e = cudaGetDevice(&d);
+  if (e != cudaSuccess) return e;
+  if (d < 0 || d >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::call_once(g_static_ws_once[d], [d]() {
+    g_static_ws_err[d] = cudaGetSymbolAddress(&g_static_ws_ptr[d], g_static_ws);
+  });
+  if (g_static_ws_err[d] != cudaSuccess) return g_static_ws_err[d];
+  *ptr = g_static_ws_ptr[d];
+  *bytes = kStaticWsBytes;
+  return cudaSuccess;
+}
 
 size_t gemm_workspace_bytes() {
   const DevInfo& dev = device_info();

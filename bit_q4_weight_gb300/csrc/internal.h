@@ -38,6 +38,10 @@ cudaError_t launch_gemm_tc(const void* w0, const void* w1, const void* x, void* 
 // partial slot and one flag word per SM (0 when the device is unusable).
 size_t gemm_workspace_bytes();
 
+// The library's own static device workspace (address on the current device,
+// looked up once per device, and its size).
+cudaError_t gemm_static_workspace(void** ptr, size_t* bytes);
+
 // Read and clear the device error word of the tcgen05 kernels (after
 // synchronising the stream) and of the GEMV kernels.
 cudaError_t read_clear_gemm_error(uint32_t* bits, cudaStream_t s);

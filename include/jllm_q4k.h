@@ -119,6 +119,21 @@ jllm_status jllm_q4k_gemm(const void* w_q4k, const void* x, void* y, jllm_dtype 
                           int64_t N, int64_t K, void* ws, size_t ws_bytes, jllm_stream_t stream);
 
 /*
+ * jllm_q4k_gemm_noalloc -- jllm_q4k_gemm with the library's own workspace.
+ * The pages describe no such call; it exists for callers that cannot hand
+ * the library device memory.  The workspace is a static device array in
+ * the library image (zero at load, ~21 MB, enough for up to 160 SMs),
+ * found with cudaGetSymbolAddress once per device; nothing is allocated.
+ * Arguments and results as jllm_q4k_gemm without ws/ws_bytes.  The array
+ * is shared by every call on a device, so calls must not overlap: issue
+ * them on one stream (or order them), as with one caller workspace.
+ * Errors: as jllm_q4k_gemm; WORKSPACE if the device has more SMs than the
+ * array was sized for.
+ */
+jllm_status jllm_q4k_gemm_noalloc(const void* w_q4k, const void* x, void* y, jllm_dtype y_dt,
+                                  int64_t M, int64_t N, int64_t K, jllm_stream_t stream);
+
+/*
  * jllm_q4k_ffn_swiglu -- h = silu(X*Wg^T) * (X*Wu^T), the gate/up half of a
  * SwiGLU MLP in one pass over X (the README's "fused ... SwiGLU", Kernels
  * bullet).  silu(z) = z / (1 + e^-z).
