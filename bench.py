@@ -3,7 +3,12 @@
 Headline: the decode sweep -- M = 1 GEMV over the seven Qwen3-4B layer shapes
 (q, k, v, o, gate, up, down) of all 36 layers, 2.04 GB of distinct seeded Q4_K
 weights resident in HBM (larger than L2, so every call streams from HBM), one
-CUDA-graph replay per step.  value = weight bytes streamed / time (GB/s).
+CUDA-graph replay per step.  The calls follow a decoder layer's data flow:
+q, k and v read one activation vector and run as one batched launch, o reads
+its own, gate and up read one (one batched launch), down its own -- four
+dependent launches per layer.  value = weight bytes streamed / time (GB/s).
+The same weights through seven single-matrix launches per layer are reported
+beside it ("decode_7call").
 Second object: the long-prompt prefill sweep at M = 2048 over the same
 weights (tcgen05 path), TFLOP/s = 2*M*N*K / time.
 
@@ -103,18 +108,54 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- our arm --
+# Groups of matrices that read one activation vector in a decoder layer.
+GROUPS = (("qkv", (0, 1, 2)), ("o", (3,)), ("ffn", (4, 5)), ("down", (6,)))
+
+
+def group_index(idx):
+    """Index in GROUPS of the group that shape `idx` belongs to."""
+    return next(gi for gi, (_, members) in enumerate(GROUPS) if idx in members)
+
+
 def build_inputs(torch, dev, layers):
-    """Seeded weights (host numpy -> device) and activations for the sweep."""
-    W, X, Y, meta = [], [], [], []
+    """Seeded weights (host numpy -> device), one activation per layer and group, outputs."""
+    W, Y, meta = [], [], []
+    XG = []  # per layer: {group: x}
     for layer in range(layers):
         for idx, (name, K, N) in enumerate(SHAPES):
             w = synthetic.q4k_weights(N, K, synthetic.weight_seed(1, layer, idx))
             W.append(torch.from_numpy(w).to(dev))
-            X.append(torch.from_numpy(synthetic.activations(1, K, synthetic.activation_seed(1, layer * 8 + idx))
-                                      .reshape(K)).to(dev))
             Y.append(torch.empty(N, dtype=torch.float32, device=dev))
             meta.append((name, K, N))
-    return W, X, Y, meta
+        xg = {}
+        for gi, (gname, members) in enumerate(GROUPS):
+            K = SHAPES[members[0]][1]
+            xg[gname] = torch.from_numpy(
+                synthetic.activations(1, K, synthetic.activation_seed(1, layer * 8 + gi)).reshape(K)).to(dev)
+        XG.append(xg)
+    return W, XG, Y, meta
+
+
+def decode_plan(W, XG, Y, meta, batched):
+    """The calls of one decode step: (weights, x, outputs, Ns, K) per launch."""
+    plan = []
+    for layer, xg in enumerate(XG):
+        base = layer * len(SHAPES)
+        for gname, members in GROUPS:
+            idx = [base + m for m in members]
+            K = meta[idx[0]][1]
+            calls = [idx] if batched else [[i] for i in idx]
+            for c in calls:
+                plan.append(([W[i] for i in c], xg[gname], [Y[i] for i in c], [meta[i][2] for i in c], K))
+    return plan
+
+
+def run_plan(q, plan):
+    for ws, x, ys, ns, K in plan:
+        if len(ws) == 1:
+            q.jllm_q4k_gemv(ws[0], x, ns[0], K, out=ys[0])
+        else:
+            q.jllm_q4k_gemv_batch(ws, x, ns, K, outs=ys)
 
 
 def time_graph(torch, graph, stream, steps, warmup):
@@ -149,24 +190,24 @@ def run_ours(args):
     import bit_q4_weight_gb300 as q
 
     layers = args.layers
-    W, X, Y, meta = build_inputs(torch, dev, layers)
+    W, XG, Y, meta = build_inputs(torch, dev, layers)
     total_bytes = sum(weight_bytes(N, K) for (_, K, N) in meta)
-    n_launch = len(meta)
+    plan = decode_plan(W, XG, Y, meta, batched=True)
+    n_launch = len(plan)
     stream = torch.cuda.Stream()
     torch.cuda.synchronize()
 
-    def sweep():
-        for w, x, y, (_, K, N) in zip(W, X, Y, meta):
-            q.jllm_q4k_gemv(w, x, N, K, out=y)
+    def capture(p):
+        with torch.cuda.stream(stream):
+            run_plan(q, p)  # eager warm-up (first launches set kernel attributes)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            run_plan(q, p)
+        torch.cuda.synchronize()
+        return g
 
-    with torch.cuda.stream(stream):
-        sweep()  # eager warm-up (first launches set kernel attributes)
-    torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=stream):
-        sweep()
-    torch.cuda.synchronize()
-
+    g = capture(plan)
     if world > 1:
         dist.barrier()
     with ClockSampler(local) as clk:
@@ -179,25 +220,26 @@ def run_ours(args):
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         t_max = float(tt.item())
     value = total_bytes * world / t_max / 1e9
+    del g
+
+    # the same weights, seven single-matrix launches per layer
+    plan7 = decode_plan(W, XG, Y, meta, batched=False)
+    g7 = capture(plan7)
+    t7 = time_graph(torch, g7, stream, args.steps, args.warmup)
+    del g7
 
     # end to end: host->device copy of every activation, the sweep, device->host of every output
-    xs_host = torch.cat([x.cpu() for x in X]).pin_memory()
+    xs_flat = [xg[gname] for xg in XG for gname, _ in GROUPS]
+    xs_host = torch.cat([x.cpu() for x in xs_flat]).pin_memory()
     ys_host = torch.empty(sum(y.numel() for y in Y), dtype=torch.float32).pin_memory()
     x_dev_all = torch.empty_like(xs_host, device=dev)
     y_dev_all = torch.empty(ys_host.numel(), dtype=torch.float32, device=dev)
-    offs_x = np.cumsum([0] + [x.numel() for x in X])
+    offs_x = np.cumsum([0] + [x.numel() for x in xs_flat])
     offs_y = np.cumsum([0] + [y.numel() for y in Y])
-    Xv = [x_dev_all[offs_x[i]:offs_x[i + 1]] for i in range(n_launch)]
-    Yv = [y_dev_all[offs_y[i]:offs_y[i + 1]] for i in range(n_launch)]
-    ge = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(stream):
-        for w, x, y, (_, K, N) in zip(W, Xv, Yv, meta):
-            q.jllm_q4k_gemv(w, x, N, K, out=y)
-    torch.cuda.synchronize()
-    with torch.cuda.graph(ge, stream=stream):
-        for w, x, y, (_, K, N) in zip(W, Xv, Yv, meta):
-            q.jllm_q4k_gemv(w, x, N, K, out=y)
-    torch.cuda.synchronize()
+    XGv = [{gname: x_dev_all[offs_x[l * len(GROUPS) + gi]:offs_x[l * len(GROUPS) + gi + 1]]
+            for gi, (gname, _) in enumerate(GROUPS)} for l in range(layers)]
+    Yv = [y_dev_all[offs_y[i]:offs_y[i + 1]] for i in range(len(Y))]
+    ge = capture(decode_plan(W, XGv, Yv, meta, batched=True))
 
     def e2e_step():
         with torch.cuda.stream(stream):
@@ -218,6 +260,7 @@ def run_ours(args):
         t_e2e = float(tt.item())
     e2e = {"value": round(total_bytes * world / t_e2e / 1e9, 2), "unit": "GB/s",
            "h2d_bytes_per_step": int(xs_host.numel() * 2), "d2h_bytes_per_step": int(ys_host.numel() * 4)}
+    del ge
 
     peaks = {}
     pk_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -229,13 +272,14 @@ def run_ours(args):
     per_shape = {}
     if args.per_shape and rank == 0:
         for idx, (name, K, N) in enumerate(SHAPES):
-            sel = [i for i in range(n_launch) if i % len(SHAPES) == idx]
+            sel = [i for i in range(len(W)) if i % len(SHAPES) == idx]
+            gname = next(gn for gn, members in GROUPS if idx in members)
             gs = torch.cuda.CUDAGraph()
             with torch.cuda.graph(gs, stream=stream):
                 for i in sel:
-                    q.jllm_q4k_gemv(W[i], X[i], N, K, out=Y[i])
+                    q.jllm_q4k_gemv(W[i], XG[i // len(SHAPES)][gname], N, K, out=Y[i])
             torch.cuda.synchronize()
-            t = time_graph(torch, gs, stream, max(3, args.steps // 2), 2)
+            t = time_graph(torch, gs, stream, max(3, args.steps // 2), 3)
             per_shape[name] = round(len(sel) * weight_bytes(N, K) / t / 1e9, 1)
             del gs
 
@@ -257,7 +301,8 @@ def run_ours(args):
             "vs_baseline": None,
             "dtype": "q4k-f16-f32",
             "data": "synthetic (seeded GGUF Q4_K blocks, fp16 N(0,1) activations)",
-            "config": {"workload": f"decode sweep M=1, {layers} layers x 7 Qwen3-4B shapes",
+            "config": {"workload": f"decode sweep M=1, {layers} layers x 7 Qwen3-4B shapes "
+                                   "(q/k/v and gate/up batched on their shared x: 4 launches per layer)",
                        "weight_bytes_per_step": total_bytes, "launches_per_step": n_launch,
                        "l2": "inputs larger than L2 (2.04 GB of weights cycled)", "parallelism": f"replicas{world}"},
             "gpu_launches": n_launch * args.steps,
@@ -267,6 +312,8 @@ def run_ours(args):
                          "traffic": None, "peak_source": peak_note,
                          "kernel": "q4k_gemv_kernel", "avg_launch_us": round(t_step / n_launch * 1e6, 3)},
             "e2e": e2e,
+            "decode_7call": {"value": round(total_bytes * world / t7 / 1e9, 2), "unit": "GB/s",
+                             "ms_per_step": round(t7 * 1e3, 4), "launches_per_step": len(plan7)},
         }
         if per_shape:
             line["per_shape_gbs"] = per_shape
@@ -331,7 +378,7 @@ def cpu_baseline(budget_s=12.0):
     for layer in range(N_LAYERS):
         for idx, (name, K, N) in enumerate(SHAPES):
             w = synthetic.q4k_weights(N, K, synthetic.weight_seed(1, layer, idx))
-            x = synthetic.activations(1, K, synthetic.activation_seed(1, layer * 8 + idx))
+            x = synthetic.activations(1, K, synthetic.activation_seed(1, layer * 8 + group_index(idx)))
             t0 = time.perf_counter()
             oracle.matmul(w, x, N, K)
             t_total += time.perf_counter() - t0
@@ -357,7 +404,7 @@ def run_reference(args):
     n_layers = min(N_LAYERS, args.warmup + args.steps)
     for layer in range(n_layers):
         inputs.append([(synthetic.q4k_weights(N, K, synthetic.weight_seed(1, layer, idx)),
-                        synthetic.activations(1, K, synthetic.activation_seed(1, layer * 8 + idx)), N, K)
+                        synthetic.activations(1, K, synthetic.activation_seed(1, layer * 8 + group_index(idx))), N, K)
                        for idx, (_, K, N) in enumerate(SHAPES)])
 
     def step(i):

@@ -134,6 +134,46 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
   }
 }
 
+// Warp-wide bounded wait: lane 0 alone polls the barrier (32 lanes polling
+// one mbarrier load the SM's barrier unit for nothing), the verdict is
+// broadcast, and __syncwarp orders the other lanes' later reads after lane
+// 0's acquire.  Must be called by all 32 lanes.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, const volatile int* abort,
+                                               uint64_t limit_ns) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait_bounded(bar, parity, abort, limit_ns) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  __syncwarp();
+  return ok != 0;
+}
+
+// As mbar_wait_warp for waits that are expected to be long (a whole tile):
+// lane 0 sleeps between polls so that the waiting warp takes no issue slots
+// or barrier-unit bandwidth from the warps doing the work.
+__device__ __forceinline__ bool mbar_wait_warp_sleepy(uint32_t bar, uint32_t parity, const volatile int* abort,
+                                                      uint64_t limit_ns) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) {
+    ok = 0;
+    if (mbar_try_wait(bar, parity)) {
+      ok = 1;
+    } else {
+      const uint64_t t0 = globaltimer_ns();
+      for (;;) {
+        __nanosleep(128);
+        if (mbar_try_wait(bar, parity)) {
+          ok = 1;
+          break;
+        }
+        if ((abort && *abort) || globaltimer_ns() - t0 > limit_ns) break;
+      }
+    }
+  }
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  __syncwarp();
+  return ok != 0;
+}
+
 // ------------------------------------------------------------------ TMA --
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

@@ -381,7 +381,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     bool ok = true;
     UnitIter it{u_begin, u_end, p.KS};
     while (ok && it.next()) {
-      ok = __all_sync(0xffffffffu, wait(b_accfull + 8 * racc.s, racc.ph));
+      ok = mbar_wait_warp_sleepy(b_accfull + 8 * racc.s, racc.ph, abort_flag, WAIT_LIMIT_NS);
       if (!ok) break;
       tc_fence_after();
       const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)racc.s * ACC_COLS;

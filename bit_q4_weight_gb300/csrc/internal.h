@@ -27,6 +27,12 @@ cudaError_t launch_dequant(const void* w, void* out, bool f16, int64_t N, int64_
 cudaError_t launch_gemv(const void* w0, const void* w1, const void* x, void* y, int64_t N, int64_t K,
                         cudaStream_t s);
 
+// Up to kMaxGemvBatch M = 1 GEMVs over the same x (and K) in one launch:
+// y[i] = fp32 [N[i]] = W[i] x.
+constexpr int kMaxGemvBatch = 8;
+cudaError_t launch_gemv_batch(const void* const* w, void* const* y, const int64_t* N, int count, const void* x,
+                              int64_t K, cudaStream_t s);
+
 // TMA + tcgen05 GEMM for any M >= 1.  w1 != nullptr selects the SwiGLU
 // epilogue (y = fp16 h).  ws (nullptr allowed) of at least
 // gemm_workspace_bytes() zero-initialised bytes enables the stream-K split.

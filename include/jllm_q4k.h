@@ -99,6 +99,25 @@ jllm_status jllm_q4k_gemv(const void* w_q4k, const void* x, float* y, int64_t N,
                           void* ws, size_t ws_bytes, jllm_stream_t stream);
 
 /*
+ * jllm_q4k_gemv_batch -- count (1..8) decode GEMVs that read the same x, in
+ * one launch: y[i][n] = sum_k x[k] * w_i[n,k] for n < N[i].  The pages name
+ * no such call; it serves the matrices of a decoder layer that share an
+ * input (q, k, v; gate, up), so that they cost one dependent launch.
+ *   w_q4k : host array of count device pointers, W_i [N[i]][K/256] blocks
+ *   y     : host array of count device pointers, [N[i]] fp32 each
+ *   N     : host array of count row counts
+ *   x     : [K] fp16, shared
+ * The host arrays are read before the call returns.  Each y[i] equals
+ * jllm_q4k_gemv(w_q4k[i], x, y[i], N[i], K) within the matmul bound (the
+ * launch configuration follows the total row count, so the fp32 summation
+ * order may differ from a single call's).
+ * Errors: INVALID_ARG (also count outside 1..8), UNSUPPORTED_SHAPE,
+ *         MISALIGNED, CUDA.
+ */
+jllm_status jllm_q4k_gemv_batch(const void* const* w_q4k, float* const* y, const int64_t* N, int count,
+                                const void* x, int64_t K, jllm_stream_t stream);
+
+/*
  * jllm_q4k_gemm -- Y[M,N] = X[M,K] * dequant(W)^T for any M >= 1.
  * (the README's "tensor-core MMQ Q4_K prefill" for M above the GEMV
  *  threshold, the GEMV kernel at or below it)

@@ -92,6 +92,30 @@ def test_other_entry_argument_errors(q):
     assert q.lib.jllm_q4k_ffn_swiglu(A, A + 4, A, A, 1, 4, 256, None, 0, None) == 3
 
 
+def test_gemv_batch_argument_errors(q):
+    import ctypes
+
+    A = ALIGNED
+    P = ctypes.c_void_p
+
+    def arrs(ws, ys, ns):
+        return (P * len(ws))(*ws), (P * len(ys))(*ys), (ctypes.c_int64 * len(ns))(*ns)
+
+    w, y, n = arrs([A, A], [A, A], [4, 8])
+    assert q.lib.jllm_q4k_gemv_batch(w, y, n, 0, A, 256, None) == 1  # count 0
+    assert q.lib.jllm_q4k_gemv_batch(w, y, n, 9, A, 256, None) == 1  # count above 8
+    assert q.lib.jllm_q4k_gemv_batch(None, y, n, 2, A, 256, None) == 1
+    assert q.lib.jllm_q4k_gemv_batch(w, y, n, 2, None, 256, None) == 1
+    assert q.lib.jllm_q4k_gemv_batch(w, y, n, 2, A, 300, None) == 2  # K % 256
+    assert q.lib.jllm_q4k_gemv_batch(w, y, n, 2, A + 2, 256, None) == 3  # x misaligned
+    w2, y2, n2 = arrs([A, None], [A, A], [4, 8])
+    assert q.lib.jllm_q4k_gemv_batch(w2, y2, n2, 2, A, 256, None) == 1  # one null W
+    w3, y3, n3 = arrs([A, A], [A, A + 4], [4, 8])
+    assert q.lib.jllm_q4k_gemv_batch(w3, y3, n3, 2, A, 256, None) == 3  # one y misaligned
+    w4, y4, n4 = arrs([A, A], [A, A], [4, 0])
+    assert q.lib.jllm_q4k_gemv_batch(w4, y4, n4, 2, A, 256, None) == 1  # N < 1
+
+
 def _no_cuda():
     try:
         import torch
