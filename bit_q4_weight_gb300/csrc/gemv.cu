@@ -192,17 +192,18 @@ __global__ void __launch_bounds__(W * 32, 512 / (W * 32)) q4k_gemv_kernel(const 
     const uint32_t bar = smem_u32(&bars[warp]);
     const uint32_t dst = smem_u32(tile + (size_t)warp * ROWS_W * srow);
     const uint32_t total = (uint32_t)rows_w * row_chunk * (SWIGLU ? 2 : 1);
+    const uint64_t pol = l2_policy_evict_first();  // weights are read once per call
     if (lane == 0) mbar_arrive_expect_tx(bar, total);
     __syncwarp();
     if (kc == NB) {
       if (lane == 0) {
-        bulk_load(dst, W0 + n_warp * row_bytes, (uint32_t)rows_w * row_chunk, bar);
-        if (SWIGLU) bulk_load(dst + RS * RP * srow, W1 + n_warp * row_bytes, (uint32_t)rows_w * row_chunk, bar);
+        bulk_load_hint(dst, W0 + n_warp * row_bytes, (uint32_t)rows_w * row_chunk, bar, pol);
+        if (SWIGLU) bulk_load_hint(dst + RS * RP * srow, W1 + n_warp * row_bytes, (uint32_t)rows_w * row_chunk, bar, pol);
       }
     } else if (lane < rows_w) {
       const int64_t off = (n_warp + lane) * row_bytes + (int64_t)kb0 * BLOCK_BYTES;
-      bulk_load(dst + lane * srow, W0 + off, row_chunk, bar);
-      if (SWIGLU) bulk_load(dst + (RS * RP + lane) * srow, W1 + off, row_chunk, bar);
+      bulk_load_hint(dst + lane * srow, W0 + off, row_chunk, bar, pol);
+      if (SWIGLU) bulk_load_hint(dst + (RS * RP + lane) * srow, W1 + off, row_chunk, bar, pol);
     }
   };
 
