@@ -263,7 +263,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------------------ MMA issuer --
+      // Descriptors are a per-stage base plus 2 per K = 16 slice (32 bytes >> 4
+      // in the start-address field, which cannot carry within shared memory),
+      // and the barriers of step k+1 are probed before step k's MMAs are issued
+      // so that the probe's latency overlaps the issue.
       const uint32_t idesc = umma_idesc_f16(TILE_N, p.BN);
+      const uint64_t adesc0 = umma_desc_sw128(sa), bdesc0 = umma_desc_sw128(sx);
+      const uint32_t a_step = (uint32_t)(NMAT * A_STAGE_BYTES) >> 4, b_step = p.x_stage_bytes >> 4;
+      constexpr uint32_t A2 = (uint32_t)A_STAGE_BYTES >> 4;  // second matrix of a SwiGLU stage
       Ring<SA> ra;
       Ring<SX> rx;
       Ring<2> racc;
@@ -276,25 +283,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)racc.s * ACC_COLS;
+        bool x_ready = mbar_try_wait(b_xfull + 8 * rx.s, rx.ph);
+        bool a_ready = mbar_try_wait(b_afull + 8 * ra.s, ra.ph);
         for (int k = it.k0; k < it.k1; ++k) {
-          if (!wait(b_xfull + 8 * rx.s, rx.ph) || !wait(b_afull + 8 * ra.s, ra.ph)) {
+          if ((!x_ready && !wait(b_xfull + 8 * rx.s, rx.ph)) || (!a_ready && !wait(b_afull + 8 * ra.s, ra.ph))) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = sa + (uint32_t)(ra.s * NMAT) * A_STAGE_BYTES;
-          const uint32_t b0 = sx + (uint32_t)rx.s * p.x_stage_bytes;
-#pragma unroll
-          for (int kk = 0; kk < KSTEP / 16; ++kk) {
-            const uint64_t bd = umma_desc_sw128(b0 + 32 * kk);
-            const uint32_t acc = (k > it.k0 || kk > 0) ? 1u : 0u;
-            umma_f16(d, umma_desc_sw128(a0 + 32 * kk), bd, idesc, acc);
-            if (SWIGLU) umma_f16(d + 128, umma_desc_sw128(a0 + A_STAGE_BYTES + 32 * kk), bd, idesc, acc);
-          }
-          umma_commit(b_aempty + 8 * ra.s);
-          umma_commit(b_xempty + 8 * rx.s);
+          const uint64_t ad = adesc0 + (uint64_t)(ra.s * a_step), bd = bdesc0 + (uint64_t)(rx.s * b_step);
+          const uint32_t sa_now = ra.s, sx_now = rx.s;
           ra.next();
           rx.next();
+          if (k + 1 < it.k1) {
+            x_ready = mbar_try_wait(b_xfull + 8 * rx.s, rx.ph);
+            a_ready = mbar_try_wait(b_afull + 8 * ra.s, ra.ph);
+          }
+          const uint32_t acc0 = k > it.k0 ? 1u : 0u;
+          umma_f16(d, ad, bd, idesc, acc0);
+          if (SWIGLU) umma_f16(d + 128, ad + A2, bd, idesc, acc0);
+#pragma unroll
+          for (int kk = 1; kk < KSTEP / 16; ++kk) {
+            umma_f16(d, ad + 2 * kk, bd + 2 * kk, idesc, 1u);
+            if (SWIGLU) umma_f16(d + 128, ad + A2 + 2 * kk, bd + 2 * kk, idesc, 1u);
+          }
+          umma_commit(b_aempty + 8 * sa_now);
+          umma_commit(b_xempty + 8 * sx_now);
         }
         if (!ok) break;
         umma_commit(b_accfull + 8 * racc.s);

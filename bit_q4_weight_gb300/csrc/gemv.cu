@@ -326,7 +326,7 @@ __global__ void __launch_bounds__(W * 32, 512 / (W * 32)) q4k_gemv_kernel(const 
 //                          0 never, 1 at entry, 2 after x staging, 3 at the end
 //   JLLM_GEMV_PRE          % of a CTA's warps whose rows are fetched before the wait
 struct Knobs {
-  int ctas_per_sm = 1;
+  int ctas_per_sm = 2;
   int R = 0, W = 0, KS = 0;
   int trigger = 1;
   int pre_pct = 100;
