@@ -43,13 +43,15 @@ M_PREFILL = 2048
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--layers", type=int, default=N_LAYERS)
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--per-shape", action="store_true", help="also time each shape alone (stderr)")
+    ap.add_argument("--per-shape", action="store_true", help="also time each shape alone")
+    ap.add_argument("--crossover", action="store_true",
+                    help="also time the GEMV (M = 1) and the tcgen05 GEMM at small M on two layer shapes")
     return ap.parse_args()
 
 
@@ -66,45 +68,66 @@ def weight_bytes(N, K):
 
 # ------------------------------------------------------------ clock sampler --
 class ClockSampler:
+    """nvidia-smi streaming SM clocks and throttle reasons every 20 ms; `mark()` brackets
+    the timed region, and only the samples read inside it are summarised."""
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index):
+    def __init__(self, index, interval_ms=20):
         self.index = index
-        self.rows = []
-        self._stop = threading.Event()
+        self.interval_ms = interval_ms
+        self.rows = []  # (host time, fields)
+        self.window = [None, None]
+        self._p = None
         self._t = None
 
-    def _run(self):
-        while not self._stop.is_set():
-            try:
-                out = subprocess.run(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
-                                      "--format=csv,noheader,nounits"], capture_output=True, text=True, timeout=5)
-                if out.returncode == 0 and out.stdout.strip():
-                    self.rows.append([c.strip() for c in out.stdout.strip().split(",")])
-            except Exception:
-                pass
-            self._stop.wait(0.2)
+    def _read(self):
+        for line in self._p.stdout:
+            f = [c.strip() for c in line.strip().split(",")]
+            if len(f) >= 9:
+                self.rows.append((time.perf_counter(), f))
 
     def __enter__(self):
-        self._t = threading.Thread(target=self._run, daemon=True)
-        self._t.start()
+        try:
+            self._p = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                                        "--format=csv,noheader,nounits", f"-lms={self.interval_ms}"],
+                                       stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+            time.sleep(0.3)  # first samples before the timed region
+        except Exception:
+            self._p = None
         return self
 
+    def mark(self, start):
+        self.window[0 if start else 1] = time.perf_counter()
+
     def __exit__(self, *a):
-        self._stop.set()
-        self._t.join(timeout=10)
+        time.sleep(2 * self.interval_ms / 1000)
+        if self._p is not None:
+            self._p.terminate()
+            try:
+                self._p.wait(timeout=5)
+            except Exception:
+                self._p.kill()
+            self._t.join(timeout=5)
 
     def summary(self):
-        if not self.rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
-        sm = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+        t0, t1 = self.window
+        rows = [f for t, f in self.rows if t0 is not None and t1 is not None and t0 <= t <= t1 + 0.03]
+        where = "timed region"
+        if not rows and self.rows:
+            rows = [min(self.rows, key=lambda r: abs(r[0] - (t0 or 0)))[1]]
+            where = "nearest sample to the timed region"
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in self.rows for i in range(4) if len(r) > 5 + i and r[5 + i] == "Active"})
+        reasons = sorted({names[i] for r in rows for i in range(4) if len(r) > 5 + i and r[5 + i] == "Active"})
         return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(self.rows)}
+                "reasons": reasons, "samples": len(rows), "window": where}
 
 
 # ---------------------------------------------------------------- our arm --
@@ -158,7 +181,7 @@ def run_plan(q, plan):
             q.jllm_q4k_gemv_batch(ws, x, ns, K, outs=ys)
 
 
-def time_graph(torch, graph, stream, steps, warmup):
+def time_graph(torch, graph, stream, steps, warmup, clk=None):
     """Seconds per replay, CUDA events recorded on the stream the graph is launched on."""
     with torch.cuda.stream(stream):
         for _ in range(warmup):
@@ -166,11 +189,15 @@ def time_graph(torch, graph, stream, steps, warmup):
         torch.cuda.synchronize()
         start = torch.cuda.Event(enable_timing=True)
         end = torch.cuda.Event(enable_timing=True)
+        if clk:
+            clk.mark(True)
         start.record(stream)
         for _ in range(steps):
             graph.replay()
         end.record(stream)
     end.synchronize()
+    if clk:
+        clk.mark(False)
     return start.elapsed_time(end) / 1e3 / steps
 
 
@@ -212,7 +239,7 @@ def run_ours(args):
         dist.barrier()
     with ClockSampler(local) as clk:
         torch.cuda.synchronize()
-        t_step = time_graph(torch, g, stream, args.steps, args.warmup)
+        t_step = time_graph(torch, g, stream, args.steps, args.warmup, clk)
     clocks = clk.summary()
     t_max = t_step
     if world > 1:
@@ -283,6 +310,10 @@ def run_ours(args):
             per_shape[name] = round(len(sel) * weight_bytes(N, K) / t / 1e9, 1)
             del gs
 
+    crossover = None
+    if args.crossover and rank == 0:
+        crossover = run_crossover(torch, q, W, meta, dev, stream, args)
+
     prefill = None
     if not args.no_prefill:
         prefill = run_prefill(torch, q, W, meta, dev, stream, args, world)
@@ -317,6 +348,8 @@ def run_ours(args):
         }
         if per_shape:
             line["per_shape_gbs"] = per_shape
+        if crossover:
+            line["crossover"] = crossover
         if prefill:
             line["prefill_m2048"] = prefill
         if not args.no_cpu_baseline and world == 1:
@@ -325,6 +358,44 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def run_crossover(torch, q, W, meta, dev, stream, args):
+    """Weight GB/s and TFLOP/s of both paths as M grows, for the q (2560->4096) and gate
+    (2560->9728) shapes over all layers: the GEMV at M = 1 and the tcgen05 GEMM at every M
+    (fp16 out, stream-K workspace) -- the evidence for the dispatch threshold."""
+    out = {}
+    for shape_idx in (0, 4):
+        name, K, N = SHAPES[shape_idx]
+        sel = [i for i in range(len(W)) if i % len(SHAPES) == shape_idx]
+        wbytes = len(sel) * weight_bytes(N, K)
+        res = {}
+        for M in (1, 2, 4, 8, 16, 33, 64, 128, 235):
+            x = torch.from_numpy(synthetic.activations(M, K, synthetic.activation_seed(2, M, shape_idx))).to(dev)
+            paths = [("gemv", None)] if M == 1 else [("gemm", q.workspace(M, N, K, dev))]
+            for path, ws in paths:
+                if path == "gemv":
+                    y = torch.empty(N, dtype=torch.float32, device=dev)
+                    call = lambda w: q.jllm_q4k_gemv(w, x.view(K), N, K, out=y)
+                else:
+                    y = torch.empty((M, N), dtype=torch.float16, device=dev)
+                    call = lambda w: q.lib.jllm_q4k_gemm(w.data_ptr(), x.data_ptr(), y.data_ptr(), 1, M, N, K,
+                                                         ws.data_ptr(), ws.numel(), stream.cuda_stream)
+                with torch.cuda.stream(stream):
+                    for i in sel:
+                        call(W[i])
+                torch.cuda.synchronize()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    for i in sel:
+                        call(W[i])
+                torch.cuda.synchronize()
+                t = time_graph(torch, g, stream, 10, 3)
+                del g
+                res[f"{path}_M{M}"] = {"weight_gbs": round(wbytes / t / 1e9, 1),
+                                       "tflops": round(2.0 * M * N * K * len(sel) / t / 1e12, 2)}
+        out[f"{name}_{K}x{N}"] = res
+    return out
 
 
 def run_prefill(torch, q, W, meta, dev, stream, args, world):
@@ -350,7 +421,7 @@ def run_prefill(torch, q, W, meta, dev, stream, args, world):
     torch.cuda.synchronize()
     steps = max(2, args.steps // 5)
     with ClockSampler(int(os.environ.get("LOCAL_RANK", "0"))) as clk:
-        t = time_graph(torch, g, stream, steps, max(1, args.warmup // 2))
+        t = time_graph(torch, g, stream, steps, max(3, args.warmup // 2), clk)
     peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
         os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
     peak = peaks.get("bf16_tflops_sustained", 1700.0)
@@ -367,6 +438,23 @@ def run_prefill(torch, q, W, meta, dev, stream, args, world):
 
 
 # ------------------------------------------------------------ CPU baseline --
+def host_cpu():
+    """CPU model and core count of this host (the oracle uses one core)."""
+    model = ""
+    try:
+        for line in open("/proc/cpuinfo"):
+            k = line.split(":")[0].strip().lower()
+            if k in ("model name", "cpu model", "hardware") and ":" in line:
+                model = line.split(":", 1)[1].strip()
+                break
+    except OSError:
+        pass
+    import platform
+
+    return {"model": model or platform.processor() or platform.machine(), "nproc": os.cpu_count(),
+            "used": "1 of %d cores" % (os.cpu_count() or 0)}
+
+
 def cpu_baseline(budget_s=12.0):
     """The oracle (single-threaded fp64 C) on the first layers of the decode sweep, bounded in time."""
     import oracle
@@ -388,7 +476,8 @@ def cpu_baseline(budget_s=12.0):
             break
     return {"value": round(done_bytes / t_total / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"decode sweep, first {layers} of 36 layers x 7 shapes ({done_bytes} weight bytes), "
-                      f"{t_total:.1f} s single-threaded fp64"}
+                      f"{t_total:.1f} s single-threaded fp64",
+            "host": host_cpu()}
 
 
 def run_reference(args):
@@ -426,7 +515,7 @@ def run_reference(args):
         "dtype": "f64", "data": "synthetic (seeded GGUF Q4_K blocks, fp16 N(0,1) activations)",
         "config": {"workload": "decode sweep M=1, one layer (7 Qwen3-4B shapes) per step, single-threaded CPU oracle"},
         "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{args.steps} layers of the decode sweep, one per step"},
+                         "sample": f"{args.steps} layers of the decode sweep, one per step", "host": host_cpu()},
         "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
