@@ -361,9 +361,10 @@ def run_ours(args):
 
 
 def run_crossover(torch, q, W, meta, dev, stream, args):
-    """Weight GB/s and TFLOP/s of both paths as M grows, for the q (2560->4096) and gate
-    (2560->9728) shapes over all layers: the GEMV at M = 1 and the tcgen05 GEMM at every M
-    (fp16 out, stream-K workspace) -- the evidence for the dispatch threshold."""
+    """Weight GB/s and TFLOP/s of jllm_q4k_gemm as M grows (fp16 out, workspace when one is
+    used), for the q (2560->4096) and gate (2560->9728) shapes over all layers, and the
+    M = 1 GEMV -- the evidence for the dispatch threshold (run once per threshold with
+    JLLM_GEMV_MAX_M to compare the two paths at the same M)."""
     out = {}
     for shape_idx in (0, 4):
         name, K, N = SHAPES[shape_idx]
@@ -379,8 +380,9 @@ def run_crossover(torch, q, W, meta, dev, stream, args):
                     call = lambda w: q.jllm_q4k_gemv(w, x.view(K), N, K, out=y)
                 else:
                     y = torch.empty((M, N), dtype=torch.float16, device=dev)
+                    wsp, wsn = (ws.data_ptr(), ws.numel()) if ws is not None else (None, 0)
                     call = lambda w: q.lib.jllm_q4k_gemm(w.data_ptr(), x.data_ptr(), y.data_ptr(), 1, M, N, K,
-                                                         ws.data_ptr(), ws.numel(), stream.cuda_stream)
+                                                         wsp, wsn, stream.cuda_stream)
                 with torch.cuda.stream(stream):
                     for i in sel:
                         call(W[i])

@@ -76,7 +76,12 @@ jllm_status check_device() {
 
 jllm_status from_cuda(cudaError_t e) { return e == cudaSuccess ? JLLM_OK : JLLM_ERR_CUDA; }
 
-int g_gemv_max_m = 1;
+// Largest M sent to the CUDA-core GEMV (the tcgen05 GEMM takes the rest).  4
+// from the measured crossover (weight GB/s on the 2560->4096 / 2560->9728
+// shapes): the GEMV is 2-4x faster up to M = 4, level at M = 8 (M = 5..8 run
+// the 8-token kernel) and slower beyond.  JLLM_GEMV_MAX_M overrides it within
+// 0..kMaxGemvTokens.
+int g_gemv_max_m = 4;
 std::once_flag g_thresh_once;
 
 int gemv_max_m() {
@@ -84,7 +89,7 @@ int gemv_max_m() {
     const char* env = getenv("JLLM_GEMV_MAX_M");
     if (env) {
       const long v = strtol(env, nullptr, 10);
-      if (v >= 0 && v <= 1) g_gemv_max_m = (int)v;
+      if (v >= 0 && v <= jllm::kMaxGemvTokens) g_gemv_max_m = (int)v;
     }
   });
   return g_gemv_max_m;
@@ -135,7 +140,7 @@ jllm_status jllm_q4k_gemv(const void* w_q4k, const void* x, float* y, int64_t N,
   if (!aligned16(w_q4k) || !aligned16(x) || !aligned16(y)) return JLLM_ERR_MISALIGNED;
   if ((st = check_workspace(ws, ws_bytes, jllm_q4k_workspace_bytes(1, N, K))) != JLLM_OK) return st;
   if ((st = check_device()) != JLLM_OK) return st;
-  return from_cuda(jllm::launch_gemv(w_q4k, nullptr, x, y, N, K, (cudaStream_t)stream));
+  return from_cuda(jllm::launch_gemv(w_q4k, nullptr, x, y, N, K, 1, false, (cudaStream_t)stream));
 }
 
 jllm_status jllm_q4k_gemv_batch(const void* const* w_q4k, float* const* y, const int64_t* N, int count,
@@ -168,8 +173,8 @@ jllm_status jllm_q4k_gemm(const void* w_q4k, const void* x, void* y, jllm_dtype 
   if ((st = check_workspace(ws, ws_bytes, jllm_q4k_workspace_bytes(M, N, K))) != JLLM_OK) return st;
   if ((st = check_device()) != JLLM_OK) return st;
   cudaStream_t s = (cudaStream_t)stream;
-  if (M <= gemv_max_m() && y_dt == JLLM_F32)
-    return from_cuda(jllm::launch_gemv(w_q4k, nullptr, x, y, N, K, s));
+  if (M <= gemv_max_m())
+    return from_cuda(jllm::launch_gemv(w_q4k, nullptr, x, y, N, K, (int)M, y_dt == JLLM_F16, s));
   return from_cuda(jllm::launch_gemm_tc(w_q4k, nullptr, x, y, y_dt == JLLM_F16, M, N, K, ws, ws_bytes, s));
 }
 
@@ -182,8 +187,8 @@ jllm_status jllm_q4k_gemm_noalloc(const void* w_q4k, const void* x, void* y, jll
   if (!aligned16(w_q4k) || !aligned16(x) || !aligned16(y)) return JLLM_ERR_MISALIGNED;
   if ((st = check_device()) != JLLM_OK) return st;
   cudaStream_t s = (cudaStream_t)stream;
-  if (M <= gemv_max_m() && y_dt == JLLM_F32)
-    return from_cuda(jllm::launch_gemv(w_q4k, nullptr, x, y, N, K, s));
+  if (M <= gemv_max_m())
+    return from_cuda(jllm::launch_gemv(w_q4k, nullptr, x, y, N, K, (int)M, y_dt == JLLM_F16, s));
   void* ws = nullptr;
   size_t ws_bytes = 0;
   cudaError_t e = jllm::gemm_static_workspace(&ws, &ws_bytes);
@@ -201,7 +206,7 @@ jllm_status jllm_q4k_ffn_swiglu(const void* w_gate, const void* w_up, const void
   if ((st = check_workspace(ws, ws_bytes, jllm_q4k_workspace_bytes(M, N, K))) != JLLM_OK) return st;
   if ((st = check_device()) != JLLM_OK) return st;
   cudaStream_t s = (cudaStream_t)stream;
-  if (M <= gemv_max_m()) return from_cuda(jllm::launch_gemv(w_gate, w_up, x, h, N, K, s));
+  if (M == 1 && gemv_max_m() >= 1) return from_cuda(jllm::launch_gemv(w_gate, w_up, x, h, N, K, 1, true, s));
   return from_cuda(jllm::launch_gemm_tc(w_gate, w_up, x, h, true, M, N, K, ws, ws_bytes, s));
 }
 

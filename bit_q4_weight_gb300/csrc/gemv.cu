@@ -133,11 +133,13 @@ struct GemvBatch {
 // Per chunk, warp w's rows arrive by bulk copy on the warp's own mbarrier --
 // a single copy when the chunk is the whole row, since the warp's rows are
 // then contiguous in W -- and each warp starts as soon as its rows land.
-template <int R, int W, int KS, bool SWIGLU>
+template <int R, int W, int KS, bool SWIGLU, int MT>
 __global__ void __launch_bounds__(W * 32, 512 / (W * 32)) q4k_gemv_kernel(const __grid_constant__ GemvBatch batch,
                                                           const uint8_t* __restrict__ W1,
                                                           const __half* __restrict__ x, int NB, int KC,
-                                                          int trigger, int pre) {
+                                                          int trigger, int pre, int M, int out_f16) {
+  // MT = tokens per launch (M <= MT rows of x, row pitch K); a lane loads each of
+  // its weight rows once per block and uses it for every token.
   // KS = K-parts: the 4 groups of a warp form 4/KS row sets x KS K-parts; part
   // p of a row set takes block pairs p, p+KS, p+2KS, ...
   constexpr int RP = SWIGLU ? R / 2 : R;  // output rows per group
@@ -164,9 +166,10 @@ __global__ void __launch_bounds__(W * 32, 512 / (W * 32)) q4k_gemv_kernel(const 
   const int64_t row_bytes = (int64_t)NB * BLOCK_BYTES;   // global row pitch
   const int srow = KC * BLOCK_BYTES;                       // shared row pitch
   uint8_t* tile = gemv_smem;                                                  // W*ROWS_W rows x KC blocks
-  uint4* xs = reinterpret_cast<uint4*>(tile + (size_t)W * ROWS_W * srow);   // KC*4 chunks of 9 units
-  float* Xs = reinterpret_cast<float*>(xs + (size_t)KC * 36);               // KC*8 sums
-  uint64_t* bars = reinterpret_cast<uint64_t*>(Xs + (size_t)KC * 8);       // W weight barriers
+  uint4* xs = reinterpret_cast<uint4*>(tile + (size_t)W * ROWS_W * srow);   // MT x KC*4 chunks of 9 units
+  float* Xs = reinterpret_cast<float*>(xs + (size_t)MT * KC * 36);          // MT x KC*8 sums
+  uint64_t* bars = reinterpret_cast<uint64_t*>(Xs + (size_t)MT * KC * 8);  // W weight barriers
+  const int64_t K = (int64_t)NB * QK;
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int grp = lane >> 3, t = lane & 7, kp = t >> 2, c = t & 3;
@@ -215,9 +218,11 @@ __global__ void __launch_bounds__(W * 32, 512 / (W * 32)) q4k_gemv_kernel(const 
   if (trigger == 1) pdl_launch_dependents();
   pdl_wait();
   if (warp >= pre) issue(0);
-  float acc[R];
+  float acc[R][MT];
 #pragma unroll
-  for (int r = 0; r < R; ++r) acc[r] = 0.f;
+  for (int r = 0; r < R; ++r)
+#pragma unroll
+    for (int m = 0; m < MT; ++m) acc[r][m] = 0.f;
   const uint8_t* wtile = tile + (size_t)warp * ROWS_W * srow;
   const uint8_t* rowp[R];
 #pragma unroll
@@ -228,29 +233,37 @@ __global__ void __launch_bounds__(W * 32, 512 / (W * 32)) q4k_gemv_kernel(const 
 
   for (int ch = 0; ch < nchunks; ++ch) {
     const int kb0 = ch * KC, kc = NB - kb0 < KC ? NB - kb0 : KC;
-    // Stage this chunk of x in the padded layout together with the sums X_j:
-    // thread i takes sub-blocks i, i + W*32, ..., XU of them with their loads
-    // in flight together.
-    for (int sb0 = threadIdx.x; sb0 < kc * 8; sb0 += XU * W * 32) {
+    // Stage this chunk of x (every token row) in the padded layout together with
+    // the sums X_j: thread i takes sub-blocks i, i + W*32, ..., XU of them with
+    // their loads in flight together.  Token rows m >= M read as zero.
+    const int nsb = kc * 8;
+    for (int sb0 = threadIdx.x; sb0 < MT * nsb; sb0 += XU * W * 32) {
       uint4 u[XU][4];
 #pragma unroll
       for (int q = 0; q < XU; ++q) {
         const int sb = sb0 + q * W * 32;
-        if (sb < kc * 8) {
-          const __half* src = x + (size_t)(kb0 + (sb >> 3)) * QK + 32 * (sb & 7);
+        const int m = MT == 1 ? 0 : sb / nsb, sl = MT == 1 ? sb : sb - m * nsb;
+        if (sb < MT * nsb) {
+          if (m < M) {
+            const __half* src = x + (size_t)m * K + (size_t)(kb0 + (sl >> 3)) * QK + 32 * (sl & 7);
 #pragma unroll
-          for (int v = 0; v < 4; ++v) u[q][v] = ldg_nc(src + 8 * v);
+            for (int v = 0; v < 4; ++v) u[q][v] = ldg_nc(src + 8 * v);
+          } else {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) u[q][v] = make_uint4(0u, 0u, 0u, 0u);
+          }
         }
       }
 #pragma unroll
       for (int q = 0; q < XU; ++q) {
         const int sb = sb0 + q * W * 32;
-        if (sb < kc * 8) {
-          const int kr = sb >> 3, j = sb & 7;
+        const int m = MT == 1 ? 0 : sb / nsb, sl = MT == 1 ? sb : sb - m * nsb;
+        if (sb < MT * nsb) {
+          const int kr = sl >> 3, j = sl & 7;
           float s = 0.f;
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
-            xs[x_unit_pos(kr, j >> 1, 4 * (j & 1) + v)] = u[q][v];
+            xs[(size_t)m * KC * 36 + x_unit_pos(kr, j >> 1, 4 * (j & 1) + v)] = u[q][v];
             const uint32_t wv[4] = {u[q][v].x, u[q][v].y, u[q][v].z, u[q][v].w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -258,7 +271,7 @@ __global__ void __launch_bounds__(W * 32, 512 / (W * 32)) q4k_gemv_kernel(const 
               s += half_hi_to_float(wv[e]);
             }
           }
-          Xs[sb] = s;
+          Xs[(size_t)m * KC * 8 + sl] = s;
         }
       }
     }
@@ -268,18 +281,23 @@ __global__ void __launch_bounds__(W * 32, 512 / (W * 32)) q4k_gemv_kernel(const 
     if (rows_w > 0) {
       if (mbar_wait_bounded(smem_u32(&bars[warp]), ch & 1, nullptr, GEMV_WAIT_LIMIT_NS)) {
         for (int kr = 2 * kpart + kp; kr < kc; kr += 2 * KS) {
-          uint4 xv[8];
-#pragma unroll
-          for (int b = 0; b < 8; ++b) xv[b] = xs[x_unit_pos(kr, c, b)];
-          const float2 X = *reinterpret_cast<const float2*>(&Xs[kr * 8 + 2 * c]);
+          RowData d[R];
 #pragma unroll
           for (int r = 0; r < R; ++r) {
             const uint8_t* blk = rowp[r] + kr * BLOCK_BYTES;
-            RowData d;
-            d.h = *reinterpret_cast<const uint4*>(blk);
-            d.q0 = *reinterpret_cast<const uint4*>(blk + 16 + 32 * c);
-            d.q1 = *reinterpret_cast<const uint4*>(blk + 32 + 32 * c);
-            acc[r] += chunk_dot(d, xv, X.x, X.y, c);
+            d[r].h = *reinterpret_cast<const uint4*>(blk);
+            d[r].q0 = *reinterpret_cast<const uint4*>(blk + 16 + 32 * c);
+            d[r].q1 = *reinterpret_cast<const uint4*>(blk + 32 + 32 * c);
+          }
+#pragma unroll
+          for (int m = 0; m < MT; ++m) {
+            const uint4* xm = xs + (size_t)m * KC * 36;
+            uint4 xv[8];
+#pragma unroll
+            for (int b = 0; b < 8; ++b) xv[b] = xm[x_unit_pos(kr, c, b)];
+            const float2 X = *reinterpret_cast<const float2*>(&Xs[(size_t)m * KC * 8 + kr * 8 + 2 * c]);
+#pragma unroll
+            for (int r = 0; r < R; ++r) acc[r][m] += chunk_dot(d[r], xv, X.x, X.y, c);
           }
         }
       } else if (lane == 0) {
@@ -295,13 +313,16 @@ __global__ void __launch_bounds__(W * 32, 512 / (W * 32)) q4k_gemv_kernel(const 
   if (trigger == 3) pdl_launch_dependents();
 #pragma unroll
   for (int r = 0; r < R; ++r) {
-    float v = acc[r];
-    v += __shfl_xor_sync(0xffffffffu, v, 1);
-    v += __shfl_xor_sync(0xffffffffu, v, 2);
-    v += __shfl_xor_sync(0xffffffffu, v, 4);
-    if (KS >= 2) v += __shfl_xor_sync(0xffffffffu, v, 8);
-    if (KS == 4) v += __shfl_xor_sync(0xffffffffu, v, 16);
-    acc[r] = v;
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+      float v = acc[r][m];
+      v += __shfl_xor_sync(0xffffffffu, v, 1);
+      v += __shfl_xor_sync(0xffffffffu, v, 2);
+      v += __shfl_xor_sync(0xffffffffu, v, 4);
+      if (KS >= 2) v += __shfl_xor_sync(0xffffffffu, v, 8);
+      if (KS == 4) v += __shfl_xor_sync(0xffffffffu, v, 16);
+      acc[r][m] = v;
+    }
   }
   if (t == 0 && kpart == 0) {
     const int64_t nb = n_warp + (int64_t)rset * RP;
@@ -310,10 +331,16 @@ __global__ void __launch_bounds__(W * 32, 512 / (W * 32)) q4k_gemv_kernel(const 
       const int64_t n = nb + i;
       if (n >= N) break;
       if (SWIGLU) {
-        const float g = acc[2 * i], u = acc[2 * i + 1];
+        const float g = acc[2 * i][0], u = acc[2 * i + 1][0];
         reinterpret_cast<__half*>(y)[n] = __float2half_rn(g / (1.0f + expf(-g)) * u);
       } else {
-        reinterpret_cast<float*>(y)[n] = acc[i];
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+          if (m < M) {
+            if (out_f16) reinterpret_cast<__half*>(y)[(size_t)m * N + n] = __float2half_rn(acc[i][m]);
+            else reinterpret_cast<float*>(y)[(size_t)m * N + n] = acc[i][m];
+          }
+        }
       }
     }
   }
@@ -343,21 +370,28 @@ const Knobs& knobs() {
   return k;
 }
 
-// Blocks per K-chunk: the whole row when the warp tiles fit `tile_cap`.
-template <int R, int W, int KS>
-int gemv_kc(int NB, size_t tile_cap) {
-  const size_t per_block = (size_t)W * (4 / KS) * R * BLOCK_BYTES;
-  size_t kc = tile_cap / per_block;
+// Shared bytes per block of K: the CTA's weight rows plus, per token, the x
+// chunk (36 units of 16 bytes) and its 8 sub-block sums.
+template <int R, int W, int KS, int MT>
+constexpr size_t gemv_bytes_per_block() {
+  return (size_t)W * (4 / KS) * R * BLOCK_BYTES + (size_t)MT * (36 * 16 + 8 * 4);
+}
+
+// Blocks per K-chunk: the whole row when it fits `cap`.
+template <int R, int W, int KS, int MT>
+int gemv_kc(int NB, size_t cap) {
+  size_t kc = cap / gemv_bytes_per_block<R, W, KS, MT>();
   if (kc < 1) kc = 1;
   return (int)(kc < (size_t)NB ? kc : (size_t)NB);
 }
 
-template <int R, int W, int KS>
+template <int R, int W, int KS, int MT>
 size_t gemv_smem_bytes(int KC) {
-  return (size_t)W * (4 / KS) * R * KC * BLOCK_BYTES + (size_t)KC * 36 * 16 + (size_t)KC * 8 * 4 + (size_t)W * 8;
+  return (size_t)KC * gemv_bytes_per_block<R, W, KS, MT>() + (size_t)W * 8;
 }
 
-constexpr size_t kGemvTileCap = 48 * 1024;
+constexpr size_t kGemvTileCap = 48 * 1024;      // weight tile of a one-token CTA
+constexpr size_t kGemvMultiCap = 100 * 1024;    // weights + x of a multi-token CTA
 
 // The matrices of a launch as the kernel sees them.
 struct GemvJob {
@@ -368,13 +402,16 @@ struct GemvJob {
   const void* w1;  // SwiGLU up matrix (count == 1), else nullptr
   const void* x;
   int64_t K;
+  int M;           // tokens (rows of x), 1..kMaxGemvTokens
+  int out_f16;
 };
 
-template <int R, int W, int KS, bool SWIGLU>
+template <int R, int W, int KS, bool SWIGLU, int MT>
 cudaError_t launch_gemv_cfg(const GemvJob& job, cudaStream_t stream, bool pdl, int trigger, int pre_pct) {
   const int NB = (int)(job.K / QK);
   constexpr int RP = SWIGLU ? R / 2 : R;
-  const int KC = gemv_kc<R, W, KS>(NB, kGemvTileCap);
+  // One token: the weight tile alone is capped; several: weights and x together.
+  const int KC = MT == 1 ? gemv_kc<R, W, KS, 0>(NB, kGemvTileCap) : gemv_kc<R, W, KS, MT>(NB, kGemvMultiCap);
   const int64_t rows_per_cta = (int64_t)(4 / KS) * RP * W;
   GemvBatch b = {};
   int64_t grid = 0;
@@ -387,8 +424,8 @@ cudaError_t launch_gemv_cfg(const GemvJob& job, cudaStream_t stream, bool pdl, i
   }
   b.count = job.count;
   if (grid > INT32_MAX) return cudaErrorInvalidValue;
-  const size_t smem = gemv_smem_bytes<R, W, KS>(KC);
-  auto kern = q4k_gemv_kernel<R, W, KS, SWIGLU>;
+  const size_t smem = gemv_smem_bytes<R, W, KS, MT>(KC);
+  auto kern = q4k_gemv_kernel<R, W, KS, SWIGLU, MT>;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -405,7 +442,7 @@ cudaError_t launch_gemv_cfg(const GemvJob& job, cudaStream_t stream, bool pdl, i
   cfg.numAttrs = pdl ? 1 : 0;
   const int pre = (W * pre_pct + 99) / 100;
   return cudaLaunchKernelEx(&cfg, kern, b, static_cast<const uint8_t*>(job.w1), static_cast<const __half*>(job.x),
-                            NB, KC, trigger, pre);
+                            NB, KC, trigger, pre, job.M, job.out_f16);
 }
 
 // The first configuration whose whole-row weight tile fits the tile cap and
@@ -429,6 +466,20 @@ int pick(const Cfg* cfgs, int n, int64_t N, int NB, int sms, int ctas_per_sm) {
   X(2, 8, 1) X(2, 4, 1) X(1, 8, 1) X(1, 4, 1) X(2, 8, 2) X(2, 4, 2) X(1, 8, 2) X(1, 4, 2)         \
       X(2, 8, 4) X(2, 4, 4) X(1, 8, 4) X(1, 4, 4) X(1, 2, 4) X(2, 2, 1) X(1, 2, 2) X(2, 2, 2)
 
+// Several tokens: one weight row per lane group (R = 1), the K split chosen
+// like the one-token configurations.
+template <int MT>
+cudaError_t run_gemv_multi(const GemvJob& job, cudaStream_t stream, bool pdl, const Knobs& kn, int64_t rows, int NB,
+                           int sms) {
+  static const Cfg cfgs[] = {{1, 4, 1}, {1, 4, 2}, {1, 4, 4}, {1, 2, 4}};
+  switch (pick<false>(cfgs, 4, rows, NB, sms, kn.ctas_per_sm)) {
+    case 0: return launch_gemv_cfg<1, 4, 1, false, MT>(job, stream, pdl, kn.trigger, kn.pre_pct);
+    case 1: return launch_gemv_cfg<1, 4, 2, false, MT>(job, stream, pdl, kn.trigger, kn.pre_pct);
+    case 2: return launch_gemv_cfg<1, 4, 4, false, MT>(job, stream, pdl, kn.trigger, kn.pre_pct);
+    default: return launch_gemv_cfg<1, 2, 4, false, MT>(job, stream, pdl, kn.trigger, kn.pre_pct);
+  }
+}
+
 cudaError_t run_gemv(const GemvJob& job, cudaStream_t stream) {
   const DevInfo& dev = device_info();
   const bool pdl = dev.pdl;
@@ -436,46 +487,53 @@ cudaError_t run_gemv(const GemvJob& job, cudaStream_t stream) {
   const Knobs& kn = knobs();
   int64_t rows = 0;
   for (int i = 0; i < job.count; ++i) rows += job.n[i];
+  if (job.M > 1) {
+    if (job.w1 != nullptr || job.count != 1) return cudaErrorInvalidValue;
+    if (job.M <= 2) return run_gemv_multi<2>(job, stream, pdl, kn, rows, NB, dev.sm_count);
+    if (job.M <= 4) return run_gemv_multi<4>(job, stream, pdl, kn, rows, NB, dev.sm_count);
+    if (job.M <= 8) return run_gemv_multi<8>(job, stream, pdl, kn, rows, NB, dev.sm_count);
+    return cudaErrorInvalidValue;
+  }
   if (job.w1 == nullptr) {
     if (kn.R) {
 #define X(R_, W_, KS_) \
-  if (kn.R == R_ && kn.W == W_ && kn.KS == KS_) return launch_gemv_cfg<R_, W_, KS_, false>(job, stream, pdl, kn.trigger, kn.pre_pct);
+  if (kn.R == R_ && kn.W == W_ && kn.KS == KS_) return launch_gemv_cfg<R_, W_, KS_, false, 1>(job, stream, pdl, kn.trigger, kn.pre_pct);
       JLLM_GEMV_CFGS(X)
 #undef X
     }
     static const Cfg cfgs[] = {{2, 8, 1}, {2, 4, 1}, {1, 4, 1}, {1, 4, 2}, {1, 4, 4}, {1, 2, 4}};
     switch (pick<false>(cfgs, 6, rows, NB, dev.sm_count, kn.ctas_per_sm)) {
-      case 0: return launch_gemv_cfg<2, 8, 1, false>(job, stream, pdl, kn.trigger, kn.pre_pct);
-      case 1: return launch_gemv_cfg<2, 4, 1, false>(job, stream, pdl, kn.trigger, kn.pre_pct);
-      case 2: return launch_gemv_cfg<1, 4, 1, false>(job, stream, pdl, kn.trigger, kn.pre_pct);
-      case 3: return launch_gemv_cfg<1, 4, 2, false>(job, stream, pdl, kn.trigger, kn.pre_pct);
-      case 4: return launch_gemv_cfg<1, 4, 4, false>(job, stream, pdl, kn.trigger, kn.pre_pct);
-      default: return launch_gemv_cfg<1, 2, 4, false>(job, stream, pdl, kn.trigger, kn.pre_pct);
+      case 0: return launch_gemv_cfg<2, 8, 1, false, 1>(job, stream, pdl, kn.trigger, kn.pre_pct);
+      case 1: return launch_gemv_cfg<2, 4, 1, false, 1>(job, stream, pdl, kn.trigger, kn.pre_pct);
+      case 2: return launch_gemv_cfg<1, 4, 1, false, 1>(job, stream, pdl, kn.trigger, kn.pre_pct);
+      case 3: return launch_gemv_cfg<1, 4, 2, false, 1>(job, stream, pdl, kn.trigger, kn.pre_pct);
+      case 4: return launch_gemv_cfg<1, 4, 4, false, 1>(job, stream, pdl, kn.trigger, kn.pre_pct);
+      default: return launch_gemv_cfg<1, 2, 4, false, 1>(job, stream, pdl, kn.trigger, kn.pre_pct);
     }
   }
   static const Cfg cfgs[] = {{4, 4, 1}, {2, 4, 1}, {2, 4, 2}, {2, 4, 4}};
   switch (pick<true>(cfgs, 4, rows, NB, dev.sm_count, kn.ctas_per_sm)) {
-    case 0: return launch_gemv_cfg<4, 4, 1, true>(job, stream, pdl, kn.trigger, kn.pre_pct);
-    case 1: return launch_gemv_cfg<2, 4, 1, true>(job, stream, pdl, kn.trigger, kn.pre_pct);
-    case 2: return launch_gemv_cfg<2, 4, 2, true>(job, stream, pdl, kn.trigger, kn.pre_pct);
-    default: return launch_gemv_cfg<2, 4, 4, true>(job, stream, pdl, kn.trigger, kn.pre_pct);
+    case 0: return launch_gemv_cfg<4, 4, 1, true, 1>(job, stream, pdl, kn.trigger, kn.pre_pct);
+    case 1: return launch_gemv_cfg<2, 4, 1, true, 1>(job, stream, pdl, kn.trigger, kn.pre_pct);
+    case 2: return launch_gemv_cfg<2, 4, 2, true, 1>(job, stream, pdl, kn.trigger, kn.pre_pct);
+    default: return launch_gemv_cfg<2, 4, 4, true, 1>(job, stream, pdl, kn.trigger, kn.pre_pct);
   }
 }
 
 }  // namespace
 
-cudaError_t launch_gemv(const void* w0, const void* w1, const void* x, void* y, int64_t N, int64_t K,
-                        cudaStream_t stream) {
+cudaError_t launch_gemv(const void* w0, const void* w1, const void* x, void* y, int64_t N, int64_t K, int M,
+                        bool y_f16, cudaStream_t stream) {
   const void* w[1] = {w0};
   void* yy[1] = {y};
   const int64_t n[1] = {N};
-  return run_gemv(GemvJob{w, yy, n, 1, w1, x, K}, stream);
+  return run_gemv(GemvJob{w, yy, n, 1, w1, x, K, M, y_f16 ? 1 : 0}, stream);
 }
 
 cudaError_t launch_gemv_batch(const void* const* w, void* const* y, const int64_t* N, int count, const void* x,
                               int64_t K, cudaStream_t stream) {
   if (count < 1 || count > kMaxGemvBatch) return cudaErrorInvalidValue;
-  return run_gemv(GemvJob{w, y, N, count, nullptr, x, K}, stream);
+  return run_gemv(GemvJob{w, y, N, count, nullptr, x, K, 1, 0}, stream);
 }
 
 cudaError_t read_clear_gemv_error(uint32_t* bits) {

@@ -22,10 +22,12 @@ const DevInfo& device_info();
 // out[N,K] = dequant(W); f16 selects fp16 output.
 cudaError_t launch_dequant(const void* w, void* out, bool f16, int64_t N, int64_t K, cudaStream_t s);
 
-// M = 1 GEMV.  w1 == nullptr: y = fp32 [N] = W0 x.  w1 != nullptr: y = fp16 [N]
-// = silu(W0 x) * (W1 x).
-cudaError_t launch_gemv(const void* w0, const void* w1, const void* x, void* y, int64_t N, int64_t K,
-                        cudaStream_t s);
+// CUDA-core GEMV for M <= kMaxGemvTokens tokens.  w1 == nullptr:
+// y[M][N] = x[M][K] W0^T, fp32 (y_f16: fp16).  w1 != nullptr (M = 1 only):
+// y = fp16 [N] = silu(W0 x) * (W1 x).
+constexpr int kMaxGemvTokens = 8;
+cudaError_t launch_gemv(const void* w0, const void* w1, const void* x, void* y, int64_t N, int64_t K, int M,
+                        bool y_f16, cudaStream_t s);
 
 // Up to kMaxGemvBatch M = 1 GEMVs over the same x (and K) in one launch:
 // y[i] = fp32 [N[i]] = W[i] x.
