@@ -135,6 +135,28 @@ class ClockSampler:
 GROUPS = (("qkv", (0, 1, 2)), ("o", (3,)), ("ffn", (4, 5)), ("down", (6,)))
 
 
+def profiled_traffic(kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary in profiles/, or None
+    when the kernel's sources no longer hash to the value recorded with the counters."""
+    import glob
+    import hashlib
+    import re
+
+    for path in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
+        for m in re.finditer(r"<!-- traffic kernel=(\S+) sources=(\S+) sha256_16=(\S+) bytes_per_launch=(\d+) -->",
+                             open(path).read()):
+            if m.group(1) != kernel:
+                continue
+            h = hashlib.sha256()
+            try:
+                for f in m.group(2).split(","):
+                    h.update(open(os.path.join(ROOT, "bit_q4_weight_gb300", "csrc", f), "rb").read())
+            except OSError:
+                return None
+            return int(m.group(4)) if h.hexdigest()[:16] == m.group(3) else None
+    return None
+
+
 def group_index(idx):
     """Index in GROUPS of the group that shape `idx` belongs to."""
     return next(gi for gi, (_, members) in enumerate(GROUPS) if idx in members)
@@ -340,7 +362,8 @@ def run_ours(args):
             "clocks": clocks,
             "roofline": {"bound": "hbm", "achieved": round(total_bytes / t_step / 1e9, 2), "peak": hbm_peak,
                          "unit": "GB/s", "frac": round(total_bytes / t_step / 1e9 / hbm_peak, 4),
-                         "traffic": None, "peak_source": peak_note,
+                         "traffic": profiled_traffic("q4k_gemv_kernel"), "peak_source": peak_note,
+                         "bytes_per_launch": round(total_bytes / n_launch),
                          "kernel": "q4k_gemv_kernel", "avg_launch_us": round(t_step / n_launch * 1e6, 3)},
             "e2e": e2e,
             "decode_7call": {"value": round(total_bytes * world / t7 / 1e9, 2), "unit": "GB/s",
@@ -433,7 +456,7 @@ def run_prefill(torch, q, W, meta, dev, stream, args, world):
             "config": {"workload": f"prefill sweep M={M}, {len(meta) // 7} layers x 7 shapes, fp16 out",
                        "flops_per_step": flops, "launches_per_step": len(meta)},
             "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": peak, "unit": "TFLOP/s",
-                         "frac": round(tf / peak, 4), "traffic": None,
+                         "frac": round(tf / peak, 4), "traffic": profiled_traffic("q4k_gemm_tc_kernel"),
                          "peak_source": "measured bf16 sustained (fp16 dense rate equal)",
                          "kernel": "q4k_gemm_tc_kernel"},
             "clocks": clk.summary()}
