@@ -337,8 +337,11 @@ def run_ours(args):
         crossover = run_crossover(torch, q, W, meta, dev, stream, args)
 
     prefill = None
+    ffn = None
     if not args.no_prefill:
         prefill = run_prefill(torch, q, W, meta, dev, stream, args, world)
+        if rank == 0:
+            ffn = run_ffn_lmhead(torch, q, W, dev, stream, args)
 
     if rank == 0:
         line = {
@@ -375,6 +378,8 @@ def run_ours(args):
             line["crossover"] = crossover
         if prefill:
             line["prefill_m2048"] = prefill
+        if ffn:
+            line["ffn_lmhead"] = ffn
         if not args.no_cpu_baseline and world == 1:
             line["cpu_baseline"] = cpu_baseline(budget_s=12.0)
         print(json.dumps(line), flush=True)
@@ -420,6 +425,44 @@ def run_crossover(torch, q, W, meta, dev, stream, args):
                 res[f"{path}_M{M}"] = {"weight_gbs": round(wbytes / t / 1e9, 1),
                                        "tflops": round(2.0 * M * N * K * len(sel) / t / 1e12, 2)}
         out[f"{name}_{K}x{N}"] = res
+    return out
+
+
+def run_ffn_lmhead(torch, q, W, dev, stream, args):
+    """Fused FFN block plus LM head: h = silu(x Wg^T) * (x Wu^T) (fp16, one pass), y = h Wd^T
+    (fp32), logits = x Wlm^T (2560 -> 151936, fp32), at M = 1 (weight GB/s) and M = 512
+    (TFLOP/s).  Gate/up/down are the first layer's weights of the sweep."""
+    K, NF = 2560, 9728
+    NL = synthetic.LM_HEAD[2]  # (name, K, N)
+    wg, wu, wd = W[4], W[5], W[6]
+    wlm = torch.from_numpy(synthetic.q4k_weights(NL, K, synthetic.weight_seed(4, 0, 7))).to(dev)
+    wbytes = 2 * weight_bytes(NF, K) + weight_bytes(K, NF) + weight_bytes(NL, K)
+    out = {}
+    for M in (1, 512):
+        x = torch.from_numpy(synthetic.activations(M, K, synthetic.activation_seed(4, M, 0))).to(dev)
+        h = torch.empty((M, NF), dtype=torch.float16, device=dev)
+        yd = torch.empty((M, K), dtype=torch.float32, device=dev)
+        ylm = torch.empty((M, NL), dtype=torch.float32, device=dev)
+
+        def step():
+            q.jllm_q4k_ffn_swiglu(wg, wu, x, NF, K, out=h)
+            q.jllm_q4k_gemm(wd, h, K, NF, out=yd)
+            q.jllm_q4k_gemm(wlm, x, NL, K, out=ylm)
+
+        with torch.cuda.stream(stream):
+            step()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step()
+        torch.cuda.synchronize()
+        t = time_graph(torch, g, stream, max(5, args.steps // 10), 3)
+        del g
+        flops = 2.0 * M * (2 * NF * K + K * NF + NL * K)
+        out[f"M{M}"] = {"us_per_step": round(t * 1e6, 1), "weight_gbs": round(wbytes / t / 1e9, 1),
+                        "tflops": round(flops / t / 1e12, 2), "launches_per_step": 3}
+    out["workload"] = ("ffn_swiglu 2560->2x9728 (fp16 h), down 9728->2560 (fp32), "
+                       "LM head 2560->151936 (fp32); weight bytes %d per step" % wbytes)
     return out
 
 
