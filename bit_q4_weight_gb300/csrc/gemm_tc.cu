@@ -35,6 +35,9 @@
 //               (fp32 / fp16) or silu(g)*u (fp16), or the fp32 partial of a
 //               cut tile.  It runs while the MMA fills the other buffer.
 // Ring positions advance by counters (stage, phase), never by division.
+// Programmatic dependent launch: setup and the first weight blocks overlap
+// the previous kernel in the stream; X is loaded and Y, the partials and the
+// flags are written only after griddepcontrol.wait.
 // Every wait is bounded; a wait that runs out sets the device error word
 // and the CTA winds down (copies and MMAs in flight are awaited, TMEM is
 // freed).
@@ -201,6 +204,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     fence_mbarrier_init();
   }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+  // Let the next kernel in the stream be scheduled (its CTAs land as SMs free up).
+  pdl_launch_dependents();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -247,6 +252,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ok = false;
             break;
           }
+          if (nx == 0) pdl_wait();  // X may come from the previous kernel; the weights do not
           mbar_arrive_expect_tx(b_xfull + 8 * rx.s, p.x_stage_bytes);
           tma_load_2d(sx + (uint32_t)rx.s * p.x_stage_bytes, &tmX, b_xfull + 8 * rx.s, k * KSTEP, m0);
           rx.next();
@@ -391,6 +397,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // Warp w reads TMEM lane quarter q = w & 3: rows 32q..32q+31 of the tile.
     const int q = warp & 3;
     const int r = 32 * q + lane;
+    pdl_wait();  // Y, the partial slots and the flags are touched only after the previous kernel
     Ring<2> racc;
     bool ok = true;
     UnitIter it{u_begin, u_end, p.KS};
@@ -464,28 +471,34 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
               for (int j = 0; j < 32; ++j) u[j] += __ldcg(slot + (size_t)j * TILE_N);
             }
-            if (n < p.N) {
-              __half* y = reinterpret_cast<__half*>(p.y);
 #pragma unroll
-              for (int j = 0; j < 32; ++j) {
-                const int m = m0 + cc + j;
-                if (cc + j < p.BN && m < p.M) y[(size_t)m * p.N + n] = __float2half_rn(a[j] / (1.0f + expf(-a[j])) * u[j]);
-              }
-            }
-          } else if (n < p.N) {
+            for (int j = 0; j < 32; ++j) a[j] = a[j] / (1.0f + expf(-a[j])) * u[j];  // h = silu(g) * u
+          }
+          // Y[m0+cc+j][n] for the j in range: one pointer step of N per token, the
+          // bounds tested once per chunk.
+          const int jv = min(32, min(p.BN - cc, p.M - (m0 + cc)));
+          if (n < p.N && jv > 0) {
+            const size_t off = (size_t)(m0 + cc) * p.N + n;
+            const size_t ld = (size_t)p.N;
             if (p.out_f16) {
-              __half* y = reinterpret_cast<__half*>(p.y);
+              __half* yp = reinterpret_cast<__half*>(p.y) + off;
+              if (jv == 32) {
 #pragma unroll
-              for (int j = 0; j < 32; ++j) {
-                const int m = m0 + cc + j;
-                if (cc + j < p.BN && m < p.M) y[(size_t)m * p.N + n] = __float2half_rn(a[j]);
+                for (int j = 0; j < 32; ++j) yp[j * ld] = __float2half_rn(a[j]);
+              } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                  if (j < jv) yp[j * ld] = __float2half_rn(a[j]);
               }
             } else {
-              float* y = reinterpret_cast<float*>(p.y);
+              float* yp = reinterpret_cast<float*>(p.y) + off;
+              if (jv == 32) {
 #pragma unroll
-              for (int j = 0; j < 32; ++j) {
-                const int m = m0 + cc + j;
-                if (cc + j < p.BN && m < p.M) y[(size_t)m * p.N + n] = a[j];
+                for (int j = 0; j < 32; ++j) yp[j * ld] = a[j];
+              } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                  if (j < jv) yp[j * ld] = a[j];
               }
             }
           }
@@ -587,11 +600,20 @@ cudaError_t launch_tc(const CUtensorMap& mx, const CUtensorMap& mw0, const CUten
   cfg.blockDim = dim3(NUM_THREADS);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
+  cudaLaunchAttribute attr[2];
+  unsigned n = 0;
+  if (cooperative) {
+    attr[n].id = cudaLaunchAttributeCooperative;
+    attr[n].val.cooperative = 1;
+    ++n;
+  }
+  if (device_info().pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = cooperative ? 1 : 0;
+  cfg.numAttrs = n;
   return cudaLaunchKernelEx(&cfg, kern, mx, mw0, mw1, p);
 }
 

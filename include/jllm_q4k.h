@@ -46,6 +46,13 @@
  * wait that runs out sets a device error word that jllm_get_device_error()
  * reads.  No call throws, prints or keeps state beyond cached device
  * properties and a per-device table of driver entry points.
+ * The GEMV and GEMM kernels are launched with programmatic dependent launch:
+ * they start fetching W while the kernel enqueued just before them on the
+ * same stream is still running, and read X / write Y (and the workspace)
+ * only after it has completed.  So W must not be written by that immediately
+ * preceding kernel (weights written earlier in the stream are fine).  Setting
+ * the environment variable JLLM_PDL=0 (read once per process) launches them
+ * without it.
  */
 #ifndef JLLM_Q4K_H
 #define JLLM_Q4K_H
