@@ -10,7 +10,9 @@ dependent launches per layer.  value = weight bytes streamed / time (GB/s).
 The same weights through seven single-matrix launches per layer are reported
 beside it ("decode_7call").
 Second object: the long-prompt prefill sweep at M = 2048 over the same
-weights (tcgen05 path), TFLOP/s = 2*M*N*K / time.
+weights (tcgen05 path), TFLOP/s = 2*M*N*K / time, in the same four launches
+per layer (q/k/v and gate/up as batched GEMMs); the seven-call sweep beside
+it ("prefill_7call").
 
 Multi-GPU: replicas only.  Each rank runs the same sweep on its own GPU with
 no collective on the data path; value = bytes all ranks streamed / max time.
@@ -467,37 +469,60 @@ def run_ffn_lmhead(torch, q, W, dev, stream, args):
 
 
 def run_prefill(torch, q, W, meta, dev, stream, args, world):
-    """M = 2048 tcgen05 GEMMs over the same resident weights, fp16 out."""
+    """M = 2048 tcgen05 GEMMs over the same resident weights, fp16 out.  The value is
+    the layer's data flow in four launches (q/k/v and gate/up each one batched GEMM
+    on their shared X, then o, then down); the seven-call sweep is timed beside it."""
     M = M_PREFILL
     xs = {}
     for (_, K, N) in meta:
         if K not in xs:
             xs[K] = torch.from_numpy(synthetic.activations(M, K, synthetic.activation_seed(3, M, K))).to(dev)
-    ys = {N: torch.empty((M, N), dtype=torch.float16, device=dev) for (_, K, N) in meta}
+    # one output per shape of a layer (k and v must not share one inside a batch)
+    ys = [torch.empty((M, N), dtype=torch.float16, device=dev) for (_, K, N) in meta[:len(SHAPES)]]
     flops = sum(2.0 * M * N * K for (_, K, N) in meta)
+    layers = len(meta) // len(SHAPES)
 
-    def sweep():
-        for w, (_, K, N) in zip(W, meta):
-            q.jllm_q4k_gemm(w, xs[K], N, K, out=ys[N])
+    def sweep7():
+        for i, (w, (_, K, N)) in enumerate(zip(W, meta)):
+            q.jllm_q4k_gemm(w, xs[K], N, K, out=ys[i % len(SHAPES)])
 
-    with torch.cuda.stream(stream):
-        sweep()
-    torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=stream):
-        sweep()
-    torch.cuda.synchronize()
-    steps = max(2, args.steps // 5)
+    def sweep_batched():
+        for layer in range(layers):
+            base = layer * len(SHAPES)
+            for _, members in GROUPS:
+                K = meta[base + members[0]][1]
+                if len(members) == 1:
+                    i = members[0]
+                    q.jllm_q4k_gemm(W[base + i], xs[K], meta[base + i][2], K, out=ys[i])
+                else:
+                    q.jllm_q4k_gemm_batch([W[base + i] for i in members], xs[K], [meta[base + i][2] for i in members],
+                                          K, outs=[ys[i] for i in members])
+
+    def timed(fn, clk=None):
+        with torch.cuda.stream(stream):
+            fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        torch.cuda.synchronize()
+        t = time_graph(torch, g, stream, max(2, args.steps // 5), max(3, args.warmup // 2), clk)
+        del g
+        return t
+
     with ClockSampler(int(os.environ.get("LOCAL_RANK", "0"))) as clk:
-        t = time_graph(torch, g, stream, steps, max(3, args.warmup // 2), clk)
+        t = timed(sweep_batched, clk)
+    t7 = timed(sweep7)
     peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
         os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
     peak = peaks.get("bf16_tflops_sustained", 1700.0)
     tf = flops / t / 1e12
-    del g
     return {"value": round(tf * world, 2), "unit": "TFLOP/s", "ms_per_step": round(t * 1e3, 3),
-            "config": {"workload": f"prefill sweep M={M}, {len(meta) // 7} layers x 7 shapes, fp16 out",
-                       "flops_per_step": flops, "launches_per_step": len(meta)},
+            "config": {"workload": f"prefill sweep M={M}, {layers} layers x 7 shapes in 4 launches per layer "
+                                   "(qkv and gate/up batched), fp16 out",
+                       "flops_per_step": flops, "launches_per_step": layers * len(GROUPS)},
+            "prefill_7call": {"value": round(flops * world / t7 / 1e12, 2), "unit": "TFLOP/s",
+                              "ms_per_step": round(t7 * 1e3, 3), "launches_per_step": len(meta)},
             "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": peak, "unit": "TFLOP/s",
                          "frac": round(tf / peak, 4), "traffic": profiled_traffic("q4k_gemm_tc_kernel"),
                          "peak_source": "measured bf16 sustained (fp16 dense rate equal)",

@@ -42,6 +42,7 @@ EXPORTS = (
     "jllm_q4k_gemv_batch",
     "jllm_q4k_gemm",
     "jllm_q4k_gemm_noalloc",
+    "jllm_q4k_gemm_batch",
     "jllm_q4k_ffn_swiglu",
     "jllm_q4k_workspace_bytes",
     "jllm_q4k_gemv_max_m",
@@ -78,6 +79,8 @@ lib.jllm_q4k_gemm.argtypes = [_P, _P, _P, ctypes.c_int, _I64, _I64, _I64, _P, _S
 lib.jllm_q4k_gemm.restype = _ST
 lib.jllm_q4k_gemm_noalloc.argtypes = [_P, _P, _P, ctypes.c_int, _I64, _I64, _I64, _P]
 lib.jllm_q4k_gemm_noalloc.restype = _ST
+lib.jllm_q4k_gemm_batch.argtypes = [_P, _P, _P, ctypes.c_int, _I64, _P, _I64, ctypes.c_int, _P, _SZ, _P]
+lib.jllm_q4k_gemm_batch.restype = _ST
 lib.jllm_q4k_ffn_swiglu.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P]
 lib.jllm_q4k_ffn_swiglu.restype = _ST
 lib.jllm_q4k_workspace_bytes.argtypes = [_I64, _I64, _I64]
@@ -274,6 +277,40 @@ def jllm_q4k_gemm_noalloc(w, x, N: int, K: int, out_dtype=None, out=None, stream
     _check(lib.jllm_q4k_gemm_noalloc(w.data_ptr(), x.data_ptr(), out.data_ptr(), dt, M, N, K, _stream_ptr(stream)),
            "jllm_q4k_gemm_noalloc")
     return out
+
+
+def jllm_q4k_gemm_batch(ws_q4k, x, Ns, K: int, out_dtype=None, outs=None, ws=None, stream=None):
+    """[Y_i[M, N_i] = X[M, K] dequant(W_i)^T] for up to 4 matrices sharing one fp16 X, one launch;
+    fp32 (default) or fp16 outputs."""
+    torch = _torch()
+    ws_q4k, Ns = list(ws_q4k), [int(n) for n in Ns]
+    if not 1 <= len(ws_q4k) <= 4 or len(Ns) != len(ws_q4k):
+        raise ValueError("1 to 4 matrices, one row count each")
+    for i, (w, n) in enumerate(zip(ws_q4k, Ns)):
+        _need(w, torch.uint8, _w_shape(n, K), f"w[{i}]")
+    if x.dim() != 2:
+        raise ValueError("x must be [M, K]")
+    M = int(x.shape[0])
+    _need(x, torch.float16, (M, K), "x")
+    out_dtype = out_dtype or (outs[0].dtype if outs else torch.float32)
+    if out_dtype not in (torch.float32, torch.float16):
+        raise TypeError("out_dtype must be torch.float32 or torch.float16")
+    if outs is None:
+        outs = [torch.empty((M, n), dtype=out_dtype, device=x.device) for n in Ns]
+    for i, (o, n) in enumerate(zip(outs, Ns)):
+        _need(o, out_dtype, (M, n), f"out[{i}]")
+    ws, nbytes = _ws(M, sum(Ns), K, ws, x.device, stream)
+    cnt = len(Ns)
+    wp = (ctypes.c_void_p * cnt)(*[w.data_ptr() for w in ws_q4k])
+    yp = (ctypes.c_void_p * cnt)(*[o.data_ptr() for o in outs])
+    npa = (ctypes.c_int64 * cnt)(*Ns)
+    dt = JLLM_F16 if out_dtype == torch.float16 else JLLM_F32
+    _check(
+        lib.jllm_q4k_gemm_batch(wp, x.data_ptr(), yp, dt, M, npa, K, cnt,
+                                ws.data_ptr() if ws is not None else None, nbytes, _stream_ptr(stream)),
+        "jllm_q4k_gemm_batch",
+    )
+    return outs
 
 
 def jllm_q4k_ffn_swiglu(w_gate, w_up, x, N: int, K: int, out=None, ws=None, stream=None):

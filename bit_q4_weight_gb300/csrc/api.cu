@@ -197,6 +197,37 @@ jllm_status jllm_q4k_gemm_noalloc(const void* w_q4k, const void* x, void* y, jll
   return from_cuda(jllm::launch_gemm_tc(w_q4k, nullptr, x, y, y_dt == JLLM_F16, M, N, K, ws, ws_bytes, s));
 }
 
+jllm_status jllm_q4k_gemm_batch(const void* const* w_q4k, const void* x, void* const* y, jllm_dtype y_dt, int64_t M,
+                                const int64_t* N, int64_t K, int count, void* ws, size_t ws_bytes,
+                                jllm_stream_t stream) {
+  if (!w_q4k || !x || !y || !N) return JLLM_ERR_INVALID_ARG;
+  if (count < 1 || count > jllm::kMaxGemmBatch) return JLLM_ERR_INVALID_ARG;
+  if (y_dt != JLLM_F32 && y_dt != JLLM_F16) return JLLM_ERR_UNSUPPORTED_DTYPE;
+  if (!aligned16(x)) return JLLM_ERR_MISALIGNED;
+  int64_t total = 0;
+  for (int i = 0; i < count; ++i) {
+    if (!w_q4k[i] || !y[i]) return JLLM_ERR_INVALID_ARG;
+    jllm_status st = check_shape(M, N[i], K);
+    if (st != JLLM_OK) return st;
+    if (!aligned16(w_q4k[i]) || !aligned16(y[i])) return JLLM_ERR_MISALIGNED;
+    total += N[i];
+  }
+  if (total > kMaxRows) return JLLM_ERR_UNSUPPORTED_SHAPE;
+  jllm_status st = check_workspace(ws, ws_bytes, jllm_q4k_workspace_bytes(M, total, K));
+  if (st != JLLM_OK) return st;
+  if ((st = check_device()) != JLLM_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  const bool f16 = y_dt == JLLM_F16;
+  if (M <= gemv_max_m()) {
+    for (int i = 0; i < count; ++i) {
+      st = from_cuda(jllm::launch_gemv(w_q4k[i], nullptr, x, y[i], N[i], K, (int)M, f16, s));
+      if (st != JLLM_OK) return st;
+    }
+    return JLLM_OK;
+  }
+  return from_cuda(jllm::launch_gemm_tc_batch(w_q4k, N, count, x, y, f16, M, K, ws, ws_bytes, s));
+}
+
 jllm_status jllm_q4k_ffn_swiglu(const void* w_gate, const void* w_up, const void* x, void* h, int64_t M,
                                 int64_t N, int64_t K, void* ws, size_t ws_bytes, jllm_stream_t stream) {
   if (!w_gate || !w_up || !x || !h) return JLLM_ERR_INVALID_ARG;

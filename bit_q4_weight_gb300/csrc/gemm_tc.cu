@@ -44,6 +44,7 @@
 #include <cudaTypedefs.h>
 
 #include <stdlib.h>
+#include <string.h>
 
 #include <mutex>
 
@@ -113,11 +114,18 @@ struct Cfg {
   static constexpr int NBARS = 2 * (SX + SA + SW) + 2 + 2 + 1;
 };
 
+// Up to kMaxGemmBatch weight matrices that share X (and so K) run in one
+// launch: matrix b owns tiles [tile0[b], tile0[b+1]) of the tile space.
+constexpr int kBatchMax = kMaxGemmBatch;
+
 struct GemmParams {
-  void* y;               // [M][N] fp32 / fp16 (h for SwiGLU)
+  void* y[kBatchMax];    // [M][N[b]] fp32 / fp16 (h for SwiGLU)
+  int N[kBatchMax];
+  int tile0[kBatchMax + 1];
+  int count;             // matrices in the batch (1 with SwiGLU: gate/up feed one output)
   float* partial;        // stream-K slots, SLOT_FLOATS per CTA (nullptr: whole tiles only)
   uint32_t* flags;       // one counter per CTA next to the slots
-  int M, N, NB;
+  int M, NB;
   int BN;                // tokens per tile, multiple of 16
   int m_tiles;           // ceil(M / BN)
   int KS;                // K steps per tile (4 per super-block)
@@ -141,6 +149,38 @@ struct Ring {
   }
 };
 
+// Tensor maps of the weight matrices: one per batch entry, or gate and up.
+struct alignas(64) WMaps {
+  CUtensorMap w[kBatchMax];
+};
+
+// Batch entry, output row and token of a tile; with all index reads on
+// constant offsets of the parameter block.
+struct TileLoc {
+  int b, n0, m0, N;
+  void* y;
+};
+__device__ __forceinline__ TileLoc locate(const GemmParams& p, int tile) {
+  TileLoc t;
+  t.b = 0;
+  t.N = p.N[0];
+  t.y = p.y[0];
+  int base = 0;
+#pragma unroll
+  for (int i = 1; i < kBatchMax; ++i)
+    if (i < p.count && tile >= p.tile0[i]) {
+      t.b = i;
+      t.N = p.N[i];
+      t.y = p.y[i];
+      base = p.tile0[i];
+    }
+  const int local = tile - base;
+  const int nt = local / p.m_tiles;
+  t.n0 = nt * TILE_N;
+  t.m0 = (local - nt * p.m_tiles) * p.BN;
+  return t;
+}
+
 __device__ __forceinline__ long long range_start(const GemmParams& p, long long g) {
   return (g * p.grains / gridDim.x) * p.grain;
 }
@@ -163,8 +203,8 @@ struct UnitIter {
 
 template <bool SWIGLU>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-    q4k_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW0,
-                       const __grid_constant__ CUtensorMap tmW1, const GemmParams p) {
+    q4k_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ WMaps tmW,
+                       const __grid_constant__ GemmParams p) {
   using C = Cfg<SWIGLU>;
   constexpr int NMAT = C::NMAT, SX = C::SX, SA = C::SA, SW = C::SW;
   extern __shared__ uint8_t gemm_smem_raw[];
@@ -225,16 +265,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (lane == 0) {
       // ---------------------------------------------------------- TMA producer --
       tma_prefetch_desc(&tmX);
-      tma_prefetch_desc(&tmW0);
-      if (SWIGLU) tma_prefetch_desc(&tmW1);
+      for (int i = 0; i < (SWIGLU ? 2 : p.count); ++i) tma_prefetch_desc(&tmW.w[i]);
       Ring<SX> rx;
       Ring<SW> rw;
       long long nx = 0, nw = 0;
       bool ok = true;
       UnitIter it{u_begin, u_end, p.KS};
       while (ok && it.next()) {
-        const int nt = it.tile / p.m_tiles;
-        const int n0 = nt * TILE_N, m0 = (it.tile - nt * p.m_tiles) * p.BN;
+        const TileLoc loc = locate(p, it.tile);
+        const int n0 = loc.n0, m0 = loc.m0;
+        const CUtensorMap* mw = &tmW.w[loc.b];
         for (int k = it.k0; k < it.k1; ++k) {
           if (k == it.k0 || (k & 3) == 0) {
             if (!wait(b_wempty + 8 * rw.s, rw.ph ^ 1u)) {
@@ -243,8 +283,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             const uint32_t bar = b_wfull + 8 * rw.s;
             mbar_arrive_expect_tx(bar, W_STAGE_BYTES * NMAT);
-            tma_load_3d(sw + (uint32_t)(rw.s * NMAT) * W_STAGE_BYTES, &tmW0, bar, 0, k >> 2, n0);
-            if (SWIGLU) tma_load_3d(sw + (uint32_t)(rw.s * NMAT + 1) * W_STAGE_BYTES, &tmW1, bar, 0, k >> 2, n0);
+            tma_load_3d(sw + (uint32_t)(rw.s * NMAT) * W_STAGE_BYTES, mw, bar, 0, k >> 2, n0);
+            if (SWIGLU) tma_load_3d(sw + (uint32_t)(rw.s * NMAT + 1) * W_STAGE_BYTES, &tmW.w[1], bar, 0, k >> 2, n0);
             rw.next();
             ++nw;
           }
@@ -406,8 +446,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!ok) break;
       tc_fence_after();
       const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)racc.s * ACC_COLS;
-      const int nt = it.tile / p.m_tiles;
-      const int n = nt * TILE_N + r, m0 = (it.tile - nt * p.m_tiles) * p.BN;
+      const TileLoc loc = locate(p, it.tile);
+      const int n = loc.n0 + r, m0 = loc.m0;
       const bool writer = it.k0 > 0;                  // later part of a cut tile
       const bool fixer = !writer && it.k1 < p.KS;      // first part of a cut tile
       constexpr int MAT_COLS = SWIGLU ? 128 : 0;       // TMEM column offset of the second matrix
@@ -477,11 +517,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           // Y[m0+cc+j][n] for the j in range: one pointer step of N per token, the
           // bounds tested once per chunk.
           const int jv = min(32, min(p.BN - cc, p.M - (m0 + cc)));
-          if (n < p.N && jv > 0) {
-            const size_t off = (size_t)(m0 + cc) * p.N + n;
-            const size_t ld = (size_t)p.N;
+          if (n < loc.N && jv > 0) {
+            const size_t off = (size_t)(m0 + cc) * loc.N + n;
+            const size_t ld = (size_t)loc.N;
             if (p.out_f16) {
-              __half* yp = reinterpret_cast<__half*>(p.y) + off;
+              __half* yp = reinterpret_cast<__half*>(loc.y) + off;
               if (jv == 32) {
 #pragma unroll
                 for (int j = 0; j < 32; ++j) yp[j * ld] = __float2half_rn(a[j]);
@@ -491,7 +531,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                   if (j < jv) yp[j * ld] = __float2half_rn(a[j]);
               }
             } else {
-              float* yp = reinterpret_cast<float*>(p.y) + off;
+              float* yp = reinterpret_cast<float*>(loc.y) + off;
               if (jv == 32) {
 #pragma unroll
                 for (int j = 0; j < 32; ++j) yp[j * ld] = a[j];
@@ -541,34 +581,36 @@ cudaError_t get_encoder(PFN_cuTensorMapEncodeTiled_v12000* out) {
   return g_encode ? cudaSuccess : cudaErrorNotSupported;
 }
 
-cudaError_t make_maps(const void* w0, const void* w1, const void* x, int64_t M, int64_t N, int64_t K, int BN,
-                      CUtensorMap* mx, CUtensorMap* mw0, CUtensorMap* mw1) {
+cudaError_t make_x_map(const void* x, int64_t M, int64_t K, int BN, CUtensorMap* mx) {
   PFN_cuTensorMapEncodeTiled_v12000 enc;
   cudaError_t e = get_encoder(&enc);
   if (e != cudaSuccess) return e;
-  {
-    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
-    const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-    const cuuint32_t box[2] = {KSTEP, (cuuint32_t)BN};
-    const cuuint32_t es[2] = {1, 1};
-    if (enc(mx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(x), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
+  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
+  const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+  const cuuint32_t box[2] = {KSTEP, (cuuint32_t)BN};
+  const cuuint32_t es[2] = {1, 1};
+  if (enc(mx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(x), dims, strides, box, es,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  return cudaSuccess;
+}
+
+// Byte view of a packed weight matrix: (144 bytes, super-block, row), one
+// super-block of 128 rows per load.
+cudaError_t make_w_map(const void* w, int64_t N, int64_t K, CUtensorMap* mw) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc;
+  cudaError_t e = get_encoder(&enc);
+  if (e != cudaSuccess) return e;
   const int64_t NB = K / QK;
   const cuuint64_t wdims[3] = {(cuuint64_t)BLOCK_BYTES, (cuuint64_t)NB, (cuuint64_t)N};
   const cuuint64_t wstrides[2] = {(cuuint64_t)BLOCK_BYTES, (cuuint64_t)(NB * BLOCK_BYTES)};
   const cuuint32_t wbox[3] = {BLOCK_BYTES, 1, TILE_N};
   const cuuint32_t wes[3] = {1, 1, 1};
-  const void* ws[2] = {w0, w1 ? w1 : w0};
-  CUtensorMap* maps[2] = {mw0, mw1};
-  for (int i = 0; i < 2; ++i) {
-    if (enc(maps[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ws[i]), wdims, wstrides, wbox, wes,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
+  if (enc(mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(w), wdims, wstrides, wbox, wes,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
   return cudaSuccess;
 }
 
@@ -590,8 +632,8 @@ const GemmKnobs& gemm_knobs() {
 }
 
 template <bool SWIGLU>
-cudaError_t launch_tc(const CUtensorMap& mx, const CUtensorMap& mw0, const CUtensorMap& mw1, const GemmParams& p,
-                      int grid, bool cooperative, size_t smem, cudaStream_t s) {
+cudaError_t launch_tc(const CUtensorMap& mx, const WMaps& mw, const GemmParams& p, int grid, bool cooperative,
+                      size_t smem, cudaStream_t s) {
   auto kern = q4k_gemm_tc_kernel<SWIGLU>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -614,7 +656,7 @@ cudaError_t launch_tc(const CUtensorMap& mx, const CUtensorMap& mw0, const CUten
   }
   cfg.attrs = attr;
   cfg.numAttrs = n;
-  return cudaLaunchKernelEx(&cfg, kern, mx, mw0, mw1, p);
+  return cudaLaunchKernelEx(&cfg, kern, mx, mw, p);
 }
 
 // Library-owned workspace of jllm_q4k_gemm_noalloc: zero at module load,
@@ -653,12 +695,18 @@ size_t gemm_workspace_bytes() {
   return (bytes + 255) & ~(size_t)255;
 }
 
-cudaError_t launch_gemm_tc(const void* w0, const void* w1, const void* x, void* y, bool y_f16, int64_t M,
-                           int64_t N, int64_t K, void* ws, size_t ws_bytes, cudaStream_t s) {
+namespace {
+
+// One launch over `count` weight matrices sharing X (count 1 with w1 set:
+// SwiGLU of gate w[0] and up w1 into one fp16 output).
+cudaError_t launch_tc_common(const void* const* w, const void* w1, const int64_t* Ns, int count, const void* x,
+                             void* const* y, bool y_f16, int64_t M, int64_t K, void* ws, size_t ws_bytes,
+                             cudaStream_t s) {
   const DevInfo& dev = device_info();
   const bool swiglu = w1 != nullptr;
   const int nmat = swiglu ? 2 : 1;
-  if (M > INT32_MAX / 2 || N > INT32_MAX / 2 || K / QK > INT32_MAX / 8) return cudaErrorInvalidValue;
+  if (count < 1 || count > kBatchMax || (swiglu && count != 1)) return cudaErrorInvalidValue;
+  if (M > INT32_MAX / 2 || K / QK > INT32_MAX / 8) return cudaErrorInvalidValue;
   const GemmKnobs& kn = gemm_knobs();
   // Tokens per tile: the whole of M up to the cap (rounded up to 16), else
   // the cap: 256, or 128 when the SwiGLU epilogue needs two accumulators.
@@ -668,15 +716,23 @@ cudaError_t launch_gemm_tc(const void* w0, const void* w1, const void* x, void* 
   if (BN > bn_cap) BN = bn_cap;
 
   GemmParams p = {};
-  p.y = y;
   p.M = (int)M;
-  p.N = (int)N;
   p.NB = (int)(K / QK);
   p.BN = BN;
   p.m_tiles = (int)((M + BN - 1) / BN);
   p.KS = 4 * p.NB;
   p.out_f16 = (y_f16 || swiglu) ? 1 : 0;
-  const long long tiles = (long long)p.m_tiles * ((N + TILE_N - 1) / TILE_N);
+  p.count = count;
+  long long tiles = 0;
+  for (int b = 0; b < count; ++b) {
+    if (Ns[b] < 1 || Ns[b] > INT32_MAX / 2) return cudaErrorInvalidValue;
+    p.y[b] = y[b];
+    p.N[b] = (int)Ns[b];
+    p.tile0[b] = (int)tiles;
+    tiles += (long long)p.m_tiles * ((Ns[b] + TILE_N - 1) / TILE_N);
+    if (tiles > INT32_MAX / 2) return cudaErrorInvalidValue;
+  }
+  p.tile0[count] = (int)tiles;
   const long long units = tiles * p.KS;
   if (units > (1ll << 53)) return cudaErrorInvalidValue;
   const int sms = dev.sm_count;
@@ -713,11 +769,26 @@ cudaError_t launch_gemm_tc(const void* w0, const void* w1, const void* x, void* 
   const size_t smem = 1024 + p.off_bar + 8 * nbars + 16;
   if (smem > dev.smem_optin) return cudaErrorInvalidValue;
 
-  CUtensorMap mx, mw0, mw1;
-  cudaError_t e = make_maps(w0, w1, x, M, N, K, BN, &mx, &mw0, &mw1);
+  CUtensorMap mx;
+  WMaps mw;
+  memset(&mw, 0, sizeof(mw));
+  cudaError_t e = make_x_map(x, M, K, BN, &mx);
+  for (int b = 0; b < count && e == cudaSuccess; ++b) e = make_w_map(w[b], Ns[b], K, &mw.w[b]);
+  if (e == cudaSuccess && swiglu) e = make_w_map(w1, Ns[0], K, &mw.w[1]);
   if (e != cudaSuccess) return e;
-  return swiglu ? launch_tc<true>(mx, mw0, mw1, p, grid, split, smem, s)
-                : launch_tc<false>(mx, mw0, mw1, p, grid, split, smem, s);
+  return swiglu ? launch_tc<true>(mx, mw, p, grid, split, smem, s) : launch_tc<false>(mx, mw, p, grid, split, smem, s);
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_tc(const void* w0, const void* w1, const void* x, void* y, bool y_f16, int64_t M,
+                           int64_t N, int64_t K, void* ws, size_t ws_bytes, cudaStream_t s) {
+  return launch_tc_common(&w0, w1, &N, 1, x, &y, y_f16, M, K, ws, ws_bytes, s);
+}
+
+cudaError_t launch_gemm_tc_batch(const void* const* w, const int64_t* N, int count, const void* x, void* const* y,
+                                 bool y_f16, int64_t M, int64_t K, void* ws, size_t ws_bytes, cudaStream_t s) {
+  return launch_tc_common(w, nullptr, N, count, x, y, y_f16, M, K, ws, ws_bytes, s);
 }
 
 cudaError_t read_clear_gemm_error(uint32_t* bits, cudaStream_t s) {

@@ -42,6 +42,12 @@ cudaError_t launch_gemv_batch(const void* const* w, void* const* y, const int64_
 cudaError_t launch_gemm_tc(const void* w0, const void* w1, const void* x, void* y, bool y_f16, int64_t M,
                            int64_t N, int64_t K, void* ws, size_t ws_bytes, cudaStream_t s);
 
+// Up to kMaxGemmBatch tcgen05 GEMMs over the same x (and K) in one
+// persistent launch: y[b] = [M][N[b]] = x W[b]^T, fp32 (y_f16: fp16).
+constexpr int kMaxGemmBatch = 4;
+cudaError_t launch_gemm_tc_batch(const void* const* w, const int64_t* N, int count, const void* x, void* const* y,
+                                 bool y_f16, int64_t M, int64_t K, void* ws, size_t ws_bytes, cudaStream_t s);
+
 // Workspace of the stream-K split on the current device: one 128 KiB fp32
 // partial slot and one flag word per SM (0 when the device is unusable).
 size_t gemm_workspace_bytes();

@@ -160,6 +160,32 @@ jllm_status jllm_q4k_gemm_noalloc(const void* w_q4k, const void* x, void* y, jll
                                   int64_t M, int64_t N, int64_t K, jllm_stream_t stream);
 
 /*
+ * jllm_q4k_gemm_batch -- count (1..4) prefill GEMMs that read the same X,
+ * in one launch: Y_i[M,N[i]] = X[M,K] * dequant(W_i)^T.  The pages name no
+ * such call; it serves the matrices of a decoder layer that share an input
+ * (q, k, v; gate, up), so that the small ones (k, v) share the SMs with
+ * the large one instead of each paying a launch and a tail.
+ *   w_q4k : host array of count device pointers, W_i [N[i]][K/256] blocks
+ *   x     : [M][K] fp16, shared
+ *   y     : host array of count device pointers, [M][N[i]] each, fp32 or
+ *           fp16 (y_dt, one type for all)
+ *   N     : host array of count row counts
+ *   ws, ws_bytes : optional workspace, sized by
+ *           jllm_q4k_workspace_bytes(M, sum N[i], K)
+ * The host arrays are read before the call returns.  M above the GEMV
+ * threshold runs one persistent tcgen05 launch over the tiles of all
+ * matrices, matrix by matrix (with a workspace the stream-K split covers
+ * them all); at or below it, one GEMV launch per matrix.  Each Y_i equals
+ * jllm_q4k_gemm(w_q4k[i], ...) within the matmul bound (the fp32
+ * summation order of cut tiles follows the batch's split).
+ * Errors: INVALID_ARG (also count outside 1..4), UNSUPPORTED_SHAPE,
+ *         MISALIGNED, UNSUPPORTED_DTYPE, WORKSPACE, CUDA.
+ */
+jllm_status jllm_q4k_gemm_batch(const void* const* w_q4k, const void* x, void* const* y, jllm_dtype y_dt,
+                                int64_t M, const int64_t* N, int64_t K, int count, void* ws,
+                                size_t ws_bytes, jllm_stream_t stream);
+
+/*
  * jllm_q4k_ffn_swiglu -- h = silu(X*Wg^T) * (X*Wu^T), the gate/up half of a
  * SwiGLU MLP in one pass over X (the README's "fused ... SwiGLU", Kernels
  * bullet).  silu(z) = z / (1 + e^-z).

@@ -116,6 +116,35 @@ def test_gemv_batch_argument_errors(q):
     assert q.lib.jllm_q4k_gemv_batch(w4, y4, n4, 2, A, 256, None) == 1  # N < 1
 
 
+def test_gemm_batch_argument_errors(q):
+    import ctypes
+
+    A = ALIGNED
+    P = ctypes.c_void_p
+
+    def arrs(ws, ys, ns):
+        return (P * len(ws))(*ws), (P * len(ys))(*ys), (ctypes.c_int64 * len(ns))(*ns)
+
+    w, y, n = arrs([A, A], [A, A], [128, 256])
+    call = q.lib.jllm_q4k_gemm_batch
+    assert call(w, A, y, 0, 64, n, 256, 0, None, 0, None) == 1  # count 0
+    assert call(w, A, y, 0, 64, n, 256, 5, None, 0, None) == 1  # count above 4
+    assert call(None, A, y, 0, 64, n, 256, 2, None, 0, None) == 1
+    assert call(w, None, y, 0, 64, n, 256, 2, None, 0, None) == 1
+    assert call(w, A, None, 0, 64, n, 256, 2, None, 0, None) == 1
+    assert call(w, A, y, 0, 64, None, 256, 2, None, 0, None) == 1
+    assert call(w, A, y, 2, 64, n, 256, 2, None, 0, None) == 4  # dtype
+    assert call(w, A, y, 0, 0, n, 256, 2, None, 0, None) == 1  # M < 1
+    assert call(w, A, y, 0, 64, n, 300, 2, None, 0, None) == 2  # K % 256
+    assert call(w, A + 2, y, 0, 64, n, 256, 2, None, 0, None) == 3  # x misaligned
+    w2, y2, n2 = arrs([A, None], [A, A], [128, 256])
+    assert call(w2, A, y2, 0, 64, n2, 256, 2, None, 0, None) == 1  # one null W
+    w3, y3, n3 = arrs([A, A], [A, A + 4], [128, 256])
+    assert call(w3, A, y3, 0, 64, n3, 256, 2, None, 0, None) == 3  # one y misaligned
+    w4, y4, n4 = arrs([A, A], [A, A], [128, 0])
+    assert call(w4, A, y4, 0, 64, n4, 256, 2, None, 0, None) == 1  # N < 1
+
+
 def _no_cuda():
     try:
         import torch
