@@ -28,7 +28,11 @@
 //    accumulated in fp32 by the mixed-precision fma.rn.f32.f16 (exact
 //    products).  Per sub-block j the offset is removed with the x sums:
 //        sum_i w_i x_i = d*sc_j * (A_j - 1024*X_j) / (1 or 16) - dmin*m_j * X_j
-//    which is the block value d*sc_j*q - dmin*m_j summed against x.
+//    which is the block value d*sc_j*q - dmin*m_j summed against x.  The
+//    6-bit sc_j and m_j of a lane's two sub-blocks come out of the packed
+//    bytes as one fp16 pair each (byte permute, masks, 1024 offset), and
+//    d*sc_j, dmin*m_j are exact fp16 x fp16 products in fp32: no integer
+//    conversions, and no lane-dependent branches.
 //  * Reduction.  Lane partials of a row are summed with xor-shuffles inside
 //    the group (deterministic order), lane 0 of the group stores y.
 //  * Launch.  With programmatic dependent launch the weight copies are issued
@@ -73,11 +77,58 @@ struct RowData {
   uint4 h, q0, q1;
 };
 
-// Partial dot product of one lane's chunk (64 weights) of one block row.
-__device__ __forceinline__ float chunk_dot(const RowData& d, const uint4 (&xv)[8], float Xlo, float Xhi,
-                                           int c) {
+__device__ __forceinline__ uint32_t prmt0(uint32_t a, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(0u), "r"(sel));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t hfma2_bits(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t r;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+  return r;
+}
+
+// Per-lane constants of the scale/min decode for chunk c (sub-blocks 2c and
+// 2c+1).  In the 12 packed bytes s[0..11] of the GGUF Q4_K layout, sub-block
+// j < 4 has sc = s[j] & 63, m = s[j+4] & 63; j >= 4 has
+// sc = (s[j+4] & 15) | (s[j-4] >> 6) << 4, m = (s[j+4] >> 4) | (s[j] >> 6) << 4.
+// Both sub-blocks of a chunk read the byte pair at offset p = 2(c & 1) of
+// s[0..3], s[4..7], s[8..11]; `sel` moves that pair into the two 16-bit
+// halves of a word, and the masks keep the fields of the lane's case.
+struct LaneDec {
+  uint32_t sel, ma, mb, mc;
+};
+__device__ __forceinline__ LaneDec lane_dec(int c) {
+  LaneDec L;
+  L.sel = (c & 1) ? 0x4342u : 0x4140u;
+  const bool hi = c >= 2;
+  L.ma = hi ? 0u : 0x003F003Fu;
+  L.mb = hi ? 0x000F000Fu : 0u;
+  L.mc = hi ? 0x00300030u : 0u;
+  return L;
+}
+
+// acc += s0*p0 + s1*p1 + t0*x0 + t1*x1 where s = d * (sc_lo, sc_hi/16) and
+// t = dmin * (-m_lo, -m_hi) are exact fp16 x fp16 products in fp32.
+__device__ __forceinline__ void scale_acc(float& acc, uint32_t dd, uint32_t sc2, uint32_t nm2, float p0, float p1,
+                                          float x0, float x1) {
+  asm("{\n .reg .b16 d0, d1, s0, s1, m0, m1;\n .reg .f32 a, b, e, f;\n"
+      " mov.b32 {d0, d1}, %1;\n mov.b32 {s0, s1}, %2;\n mov.b32 {m0, m1}, %3;\n"
+      " fma.rn.f32.f16 a, d0, s0, %8;\n fma.rn.f32.f16 b, d0, s1, %8;\n"
+      " fma.rn.f32.f16 e, d1, m0, %8;\n fma.rn.f32.f16 f, d1, m1, %8;\n"
+      " fma.rn.f32 %0, a, %4, %0;\n fma.rn.f32 %0, b, %5, %0;\n"
+      " fma.rn.f32 %0, e, %6, %0;\n fma.rn.f32 %0, f, %7, %0;\n}"
+      : "+f"(acc)
+      : "r"(dd), "r"(sc2), "r"(nm2), "f"(p0), "f"(p1), "f"(x0), "f"(x1), "f"(0.f));
+}
+
+// acc += partial dot product of one lane's chunk (64 weights) of one block row.
+__device__ __forceinline__ void chunk_dot(float& acc, const RowData& d, const uint4 (&xv)[8], float Xlo, float Xhi,
+                                          const LaneDec& L) {
   const uint32_t qw[8] = {d.q0.x, d.q0.y, d.q0.z, d.q0.w, d.q1.x, d.q1.y, d.q1.z, d.q1.w};
-  float alo0 = 0.f, alo1 = 0.f, ahi0 = 0.f, ahi1 = 0.f;
+  // The 1024 offset of the codes is taken out up front: A_j starts at -1024 X_j.
+  float alo0 = -1024.f * Xlo, alo1 = 0.f, ahi0 = -1024.f * Xhi, ahi1 = 0.f;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const uint32_t w = qw[i];
@@ -98,22 +149,20 @@ __device__ __forceinline__ float chunk_dot(const RowData& d, const uint4 (&xv)[8
       fma4_h(ahi0, h02, h13, xha, xhb);
     }
   }
-  const float alo = alo0 + alo1, ahi = ahi0 + ahi1;
-  // scales and mins of sub-blocks 2c (lo) and 2c+1 (hi)
-  const int hi = c >> 1, sh = 16 * (c & 1);
-  const uint32_t A = d.h.y >> sh, B = d.h.z >> sh, E = d.h.w >> sh;
-  const uint32_t sc_lo = hi ? ((E & 15u) | ((A >> 2) & 0x30u)) : (A & 63u);
-  const uint32_t sc_hi = hi ? (((E >> 8) & 15u) | ((A >> 10) & 0x30u)) : ((A >> 8) & 63u);
-  const uint32_t m_lo = hi ? (((E >> 4) & 15u) | ((B >> 2) & 0x30u)) : (B & 63u);
-  const uint32_t m_hi = hi ? (((E >> 12) & 15u) | ((B >> 10) & 0x30u)) : ((B >> 8) & 63u);
-  const float dd = half_lo_to_float(d.h.x), dm = half_hi_to_float(d.h.x);
-  const float s_lo = dd * (float)sc_lo, s_hi = dd * (float)sc_hi * 0.0625f;
-  const float t_lo = dm * (float)m_lo, t_hi = dm * (float)m_hi;
-  float r = s_lo * fmaf(-1024.f, Xlo, alo);
-  r = fmaf(-t_lo, Xlo, r);
-  r = fmaf(s_hi, fmaf(-1024.f, Xhi, ahi), r);
-  r = fmaf(-t_hi, Xhi, r);
-  return r;
+  // Scales and mins of sub-blocks 2c (lo half) and 2c+1 (hi half), as fp16
+  // 1024+v, then exact fp16 values: (sc_lo, sc_hi/16) and (-m_lo, -m_hi).
+  const uint32_t py = prmt0(d.h.y, L.sel), pz = prmt0(d.h.z, L.sel), pw = prmt0(d.h.w, L.sel);
+  uint32_t scw = lop3_and_or(py, L.ma, 0x64006400u);
+  scw = lop3_and_or(pw, L.mb, scw);
+  scw = lop3_and_or(py >> 2, L.mc, scw);
+  uint32_t mw = lop3_and_or(pz, L.ma, 0x64006400u);
+  mw = lop3_and_or(pw >> 4, L.mb, mw);
+  mw = lop3_and_or(pz >> 2, L.mc, mw);
+  const uint32_t sc2 = hfma2_bits(scw, 0x2C003C00u, 0xD400E400u);  // * (1, 1/16) + (-1024, -64)
+  const uint32_t nm2 = hfma2_bits(mw, 0xBC00BC00u, 0x64006400u);   // * (-1, -1) + (1024, 1024)
+  //   sum_i w_i x_i = d*sc_lo * (A_lo - 1024 X_lo) + d*sc_hi/16 * (A_hi - 1024 X_hi)
+  //                   - dmin*m_lo * X_lo - dmin*m_hi * X_hi
+  scale_acc(acc, d.h.x, sc2, nm2, alo0 + alo1, ahi0 + ahi1, Xlo, Xhi);
 }
 
 __device__ uint32_t g_gemv_error;
@@ -174,6 +223,7 @@ __global__ void __launch_bounds__(W * 32, 512 / (W * 32)) q4k_gemv_kernel(const 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int grp = lane >> 3, t = lane & 7, kp = t >> 2, c = t & 3;
   const int rset = grp / KS, kpart = grp % KS;
+  const LaneDec L = lane_dec(c);
   const int64_t n_cta = (int64_t)((int)blockIdx.x - cta0) * (W * RS * RP);
   const int64_t n_warp = n_cta + (int64_t)warp * RS * RP;
   const int rows_w = (int)(N - n_warp < RS * RP ? (N - n_warp > 0 ? N - n_warp : 0) : RS * RP);
@@ -297,7 +347,7 @@ __global__ void __launch_bounds__(W * 32, 512 / (W * 32)) q4k_gemv_kernel(const 
             for (int b = 0; b < 8; ++b) xv[b] = xm[x_unit_pos(kr, c, b)];
             const float2 X = *reinterpret_cast<const float2*>(&Xs[(size_t)m * KC * 8 + kr * 8 + 2 * c]);
 #pragma unroll
-            for (int r = 0; r < R; ++r) acc[r][m] += chunk_dot(d[r], xv, X.x, X.y, c);
+            for (int r = 0; r < R; ++r) chunk_dot(acc[r][m], d[r], xv, X.x, X.y, L);
           }
         }
       } else if (lane == 0) {
