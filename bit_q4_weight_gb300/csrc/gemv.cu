@@ -61,6 +61,14 @@ __device__ __forceinline__ void fma4_h(float& acc, uint32_t w0, uint32_t w1, uin
       : "r"(w0), "r"(w1), "r"(xa), "r"(xb));
 }
 
+// acc += lo + hi of an fp16 pair, each added exactly widened (fp16 * 1 + fp32).
+__device__ __forceinline__ void add_halves(float& acc, uint32_t h2) {
+  asm("{\n .reg .b16 a, b, one;\n mov.b32 {a, b}, %1;\n mov.b16 one, 0x3C00;\n"
+      " fma.rn.f32.f16 %0, a, one, %0;\n fma.rn.f32.f16 %0, b, one, %0;\n}"
+      : "+f"(acc)
+      : "r"(h2));
+}
+
 __device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t mask, uint32_t orv) {
   uint32_t r;
   asm("lop3.b32 %0, %1, %2, %3, 0xea;" : "=r"(r) : "r"(a), "r"(mask), "r"(orv));  // (a & b) | c
@@ -310,18 +318,17 @@ __global__ void __launch_bounds__(W * 32, 512 / (W * 32)) q4k_gemv_kernel(const 
         const int m = MT == 1 ? 0 : sb / nsb, sl = MT == 1 ? sb : sb - m * nsb;
         if (sb < MT * nsb) {
           const int kr = sl >> 3, j = sl & 7;
-          float s = 0.f;
+          // X_j in fp32: four chains of fp16 * 1 + fp32 (exact conversions)
+          float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
             xs[(size_t)m * KC * 36 + x_unit_pos(kr, j >> 1, 4 * (j & 1) + v)] = u[q][v];
-            const uint32_t wv[4] = {u[q][v].x, u[q][v].y, u[q][v].z, u[q][v].w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              s += half_lo_to_float(wv[e]);
-              s += half_hi_to_float(wv[e]);
-            }
+            add_halves(s4[v], u[q][v].x);
+            add_halves(s4[v], u[q][v].y);
+            add_halves(s4[v], u[q][v].z);
+            add_halves(s4[v], u[q][v].w);
           }
-          Xs[(size_t)m * KC * 8 + sl] = s;
+          Xs[(size_t)m * KC * 8 + sl] = (s4[0] + s4[1]) + (s4[2] + s4[3]);
         }
       }
     }
