@@ -340,10 +340,15 @@ def run_ours(args):
 
     prefill = None
     ffn = None
+    short = None
     if not args.no_prefill:
         prefill = run_prefill(torch, q, W, meta, dev, stream, args, world)
         if rank == 0:
             ffn = run_ffn_lmhead(torch, q, W, dev, stream, args)
+            short = {f"M{m}": run_prefill(torch, q, W, meta, dev, stream, args, world, M=m, short=True)
+                     for m in (33, 235)}
+            short["workload"] = ("short-prompt prefill over the decode sweep's weights, per-token scaled X, "
+                                 "fp16 out, 4 launches per layer (qkv and gate/up batched)")
 
     if rank == 0:
         line = {
@@ -380,6 +385,8 @@ def run_ours(args):
             line["crossover"] = crossover
         if prefill:
             line["prefill_m2048"] = prefill
+            if short:
+                line["prefill_short"] = short
         if ffn:
             line["ffn_lmhead"] = ffn
         if not args.no_cpu_baseline and world == 1:
@@ -463,20 +470,35 @@ def run_ffn_lmhead(torch, q, W, dev, stream, args):
         flops = 2.0 * M * (2 * NF * K + K * NF + NL * K)
         out[f"M{M}"] = {"us_per_step": round(t * 1e6, 1), "weight_gbs": round(wbytes / t / 1e9, 1),
                         "tflops": round(flops / t / 1e12, 2), "launches_per_step": 3}
+        if M == 1:
+            # the LM head alone: one large independent GEMV launch, the kernel's sustained rate
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                q.jllm_q4k_gemm(wlm, x, NL, K, out=ylm)
+            torch.cuda.synchronize()
+            tl = time_graph(torch, g, stream, max(5, args.steps // 10), 3)
+            del g
+            lb = weight_bytes(NL, K)
+            peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
+                os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
+            hbm = peaks.get("hbm_gbs", 6800.0)
+            out["lm_head_M1"] = {"us": round(tl * 1e6, 1), "weight_gbs": round(lb / tl / 1e9, 1),
+                                 "frac_of_hbm": round(lb / tl / 1e9 / hbm, 4)}
     out["workload"] = ("ffn_swiglu 2560->2x9728 (fp16 h), down 9728->2560 (fp32), "
                        "LM head 2560->151936 (fp32); weight bytes %d per step" % wbytes)
     return out
 
 
-def run_prefill(torch, q, W, meta, dev, stream, args, world):
+def run_prefill(torch, q, W, meta, dev, stream, args, world, M=M_PREFILL, short=False):
     """M = 2048 tcgen05 GEMMs over the same resident weights, fp16 out.  The value is
     the layer's data flow in four launches (q/k/v and gate/up each one batched GEMM
-    on their shared X, then o, then down); the seven-call sweep is timed beside it."""
-    M = M_PREFILL
+    on their shared X, then o, then down); the seven-call sweep is timed beside it.
+    short=True: the short-prompt sizes (M = 33, 235) with per-token scaled X."""
     xs = {}
     for (_, K, N) in meta:
         if K not in xs:
-            xs[K] = torch.from_numpy(synthetic.activations(M, K, synthetic.activation_seed(3, M, K))).to(dev)
+            seed = synthetic.activation_seed(2 if short else 3, M, K)
+            xs[K] = torch.from_numpy(synthetic.activations(M, K, seed, per_token_scale=short)).to(dev)
     # one output per shape of a layer (k and v must not share one inside a batch)
     ys = [torch.empty((M, N), dtype=torch.float16, device=dev) for (_, K, N) in meta[:len(SHAPES)]]
     flops = sum(2.0 * M * N * K for (_, K, N) in meta)
@@ -510,6 +532,13 @@ def run_prefill(torch, q, W, meta, dev, stream, args, world):
         del g
         return t
 
+    if short:
+        t, t7 = timed(sweep_batched), timed(sweep7)
+        wb = sum(weight_bytes(N, K) for (_, K, N) in meta)
+        return {"M": M, "us_per_step": round(t * 1e6, 1), "weight_gbs": round(wb / t / 1e9, 1),
+                "tflops": round(flops / t / 1e12, 2), "launches_per_step": layers * len(GROUPS),
+                "seven_call": {"us_per_step": round(t7 * 1e6, 1), "weight_gbs": round(wb / t7 / 1e9, 1),
+                               "tflops": round(flops / t7 / 1e12, 2)}}
     with ClockSampler(int(os.environ.get("LOCAL_RANK", "0"))) as clk:
         t = timed(sweep_batched, clk)
     t7 = timed(sweep7)

@@ -150,7 +150,7 @@ struct Ring {
 };
 
 // Tensor maps of the weight matrices: one per batch entry, or gate and up.
-struct alignas(64) WMaps {
+struct WMaps {
   CUtensorMap w[kBatchMax];
 };
 
