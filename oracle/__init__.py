@@ -16,6 +16,9 @@ Every function restates a definition in plain single-threaded C, fp64:
   "tensor-core MMQ Q4_K prefill" of the README's Kernels bullet).
 * ``swiglu`` -- h = silu(g) * u, silu(z) = z / (1 + e^-z) (the SwiGLU of the
   README's "fused RMSNorm + RoPE + SwiGLU" kernel).
+* ``rmsnorm`` -- xn = x * gamma / sqrt(mean(x^2) + eps) per token row (the
+  RMSNorm of the same kernel bullet; the standard root-mean-square norm, named
+  but not printed on the pages), the prologue of the fused-norm GEMV.
 * ``quantize`` -- a plain non-iterative quantiser used only for the round-trip
   pin (not on the pages; the rule is stated in q4k_oracle.c).
 
@@ -74,6 +77,8 @@ def _load():
     lib.oq_matmul_cols.restype = ctypes.c_int
     lib.oq_swiglu.argtypes = [P, P, I64, P]
     lib.oq_swiglu.restype = None
+    lib.oq_rmsnorm.argtypes = [P, P, I64, I64, ctypes.c_double, P]
+    lib.oq_rmsnorm.restype = None
     lib.oq_quantize_block.argtypes = [P, P]
     lib.oq_quantize_block.restype = None
     lib.oq_quantize.argtypes = [P, I64, I64, P]
@@ -193,6 +198,16 @@ def swiglu(g: np.ndarray, u: np.ndarray) -> np.ndarray:
     h = np.empty(g.shape, dtype=np.float64)
     _load().oq_swiglu(_ptr(g), _ptr(u), g.size, _ptr(h))
     return h
+
+
+def rmsnorm(x: np.ndarray, gamma: np.ndarray, eps: float) -> np.ndarray:
+    """xn = x * gamma / sqrt(mean(x^2) + eps) per row, fp64 ([M, K] or [K])."""
+    gamma = np.ascontiguousarray(gamma, dtype=np.float64).reshape(-1)
+    K = gamma.size
+    xa = np.ascontiguousarray(np.asarray(x, dtype=np.float64).reshape(-1, K))
+    out = np.empty_like(xa)
+    _load().oq_rmsnorm(_ptr(xa), _ptr(gamma), xa.shape[0], K, float(eps), _ptr(out))
+    return out.reshape(np.asarray(x).shape)
 
 
 def quantize(w: np.ndarray) -> np.ndarray:

@@ -229,6 +229,22 @@ void oq_swiglu(const double* g, const double* u, int64_t n, double* h) {
   for (int64_t i = 0; i < n; i++) h[i] = g[i] / (1.0 + exp(-g[i])) * u[i];
 }
 
+/* -------------------------------------------------------------- RMSNorm --- */
+
+/* xn[m][k] = x[m][k] * gamma[k] / sqrt(mean_k x[m][k]^2 + eps) for each of the
+ * M rows of K values, fp64, k ascending (the "RMSNorm" of the README's "fused
+ * RMSNorm + RoPE + SwiGLU" kernel; the formula is the standard root-mean-square
+ * layer norm, which the pages name but do not print). */
+void oq_rmsnorm(const double* x, const double* gamma, int64_t M, int64_t K, double eps, double* xn) {
+  for (int64_t m = 0; m < M; m++) {
+    const double* xr = x + m * K;
+    double ss = 0.0;
+    for (int64_t k = 0; k < K; k++) ss += xr[k] * xr[k];
+    const double r = 1.0 / sqrt(ss / (double)K + eps);
+    for (int64_t k = 0; k < K; k++) xn[m * K + k] = xr[k] * r * gamma[k];
+  }
+}
+
 /* ------------------------------------------------------------ quantiser --- */
 
 /* Smallest binary16 value >= v (v >= 0, finite, below 65504), as bits. */

@@ -341,6 +341,38 @@ def test_swiglu_against_closed_forms():
 
 # ------------------------------------------------------- synthetic inputs ----
 
+def test_rmsnorm_against_closed_forms():
+    # (3, 4): mean square 12.5, root 5/sqrt(2): outputs 3*sqrt(2)/5 and 4*sqrt(2)/5
+    xn = oracle.rmsnorm(np.array([3.0, 4.0]), np.ones(2), 0.0)
+    assert np.allclose(xn, [3 * math.sqrt(2) / 5, 4 * math.sqrt(2) / 5], rtol=1e-15, atol=0)
+    # a constant row normalises to its sign, whatever the constant (exactly for powers of two)
+    for c in (-0.25, 4096.0):
+        assert np.array_equal(oracle.rmsnorm(np.full(256, c), np.ones(256), 0.0), np.full(256, math.copysign(1.0, c)))
+    for c in (-7.5, 0.001, 3e4):
+        xn = oracle.rmsnorm(np.full(256, c), np.ones(256), 0.0)
+        assert np.allclose(xn, math.copysign(1.0, c), rtol=1e-14, atol=0)
+    # eps sits under the root: 1 / sqrt(1 + 3) = 0.5
+    assert oracle.rmsnorm(np.array([1.0]), np.ones(1), 3.0)[0] == 0.5
+    # an all-zero row stays zero (no 0/0) when eps > 0
+    assert np.array_equal(oracle.rmsnorm(np.zeros(64), np.ones(64), 1e-6), np.zeros(64))
+
+
+def test_rmsnorm_invariants():
+    rng = np.random.Generator(np.random.PCG64(77))
+    x = rng.standard_normal((5, 512)) * rng.uniform(0.1, 10.0, size=(5, 1))
+    g = rng.uniform(-2.0, 2.0, size=512)
+    one = oracle.rmsnorm(x, np.ones(512), 0.0)
+    # unit root-mean-square per row with gamma = 1 and eps = 0
+    assert np.allclose(np.mean(one**2, axis=1), 1.0, rtol=1e-13)
+    # invariant to a positive scale of the row
+    assert np.allclose(oracle.rmsnorm(x * 37.0, np.ones(512), 0.0), one, rtol=1e-13, atol=1e-15)
+    # gamma scales each column
+    assert np.allclose(oracle.rmsnorm(x, g, 0.0), one * g, rtol=1e-13, atol=1e-15)
+    # rows are independent: the batch equals the row-by-row results
+    for m in range(5):
+        assert np.array_equal(oracle.rmsnorm(x[m:m + 1], g, 1e-6)[0], oracle.rmsnorm(x[m], g, 1e-6))
+
+
 def test_synthetic_weights_distribution():
     w = synthetic.q4k_weights(64, 2560, seed=1)
     assert w.shape == (64, 10 * 144)
