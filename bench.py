@@ -279,6 +279,35 @@ def run_ours(args):
     t7 = time_graph(torch, g7, stream, args.steps, args.warmup)
     del g7
 
+    # the same batched sweep with the RMSNorm prologue on the q/k/v and gate/up launches
+    # (their x is then the un-normalised residual stream; one fp32 gamma per group and layer)
+    gammas = [{gname: torch.from_numpy(np.random.Generator(np.random.PCG64(7000 + 4 * l + gi))
+                                       .uniform(0.25, 2.0, size=meta[l * len(SHAPES) + members[0]][1])
+                                       .astype(np.float32)).to(dev)
+               for gi, (gname, members) in enumerate(GROUPS) if len(members) > 1} for l in range(layers)]
+    plan_n = []
+    for (ws, x, ys, ns, K), (layer, gname) in zip(plan, [(l, gn) for l in range(layers) for gn, _ in GROUPS]):
+        plan_n.append((ws, x, ys, ns, K, gammas[layer].get(gname)))
+
+    def run_plan_norm():
+        for ws, x, ys, ns, K, gm in plan_n:
+            if gm is not None:
+                q.jllm_q4k_gemv_rmsnorm_batch(ws, x, gm, 1e-6, ns, K, outs=ys)
+            elif len(ws) == 1:
+                q.jllm_q4k_gemv(ws[0], x, ns[0], K, out=ys[0])
+            else:
+                q.jllm_q4k_gemv_batch(ws, x, ns, K, outs=ys)
+
+    with torch.cuda.stream(stream):
+        run_plan_norm()
+    torch.cuda.synchronize()
+    gn = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gn, stream=stream):
+        run_plan_norm()
+    torch.cuda.synchronize()
+    tn = time_graph(torch, gn, stream, args.steps, args.warmup)
+    del gn
+
     # end to end: host->device copy of every activation, the sweep, device->host of every output
     xs_flat = [xg[gname] for xg in XG for gname, _ in GROUPS]
     xs_host = torch.cat([x.cpu() for x in xs_flat]).pin_memory()
@@ -378,6 +407,10 @@ def run_ours(args):
             "e2e": e2e,
             "decode_7call": {"value": round(total_bytes * world / t7 / 1e9, 2), "unit": "GB/s",
                              "ms_per_step": round(t7 * 1e3, 4), "launches_per_step": len(plan7)},
+            "decode_rmsnorm_fused": {"value": round(total_bytes * world / tn / 1e9, 2), "unit": "GB/s",
+                                     "ms_per_step": round(tn * 1e3, 4), "launches_per_step": len(plan_n),
+                                     "workload": "the batched decode sweep with RMSNorm(x) in the prologue of "
+                                                 "the q/k/v and gate/up launches"},
         }
         if per_shape:
             line["per_shape_gbs"] = per_shape

@@ -40,6 +40,7 @@ EXPORTS = (
     "jllm_q4k_dequant",
     "jllm_q4k_gemv",
     "jllm_q4k_gemv_batch",
+    "jllm_q4k_gemv_rmsnorm_batch",
     "jllm_q4k_gemm",
     "jllm_q4k_gemm_noalloc",
     "jllm_q4k_gemm_batch",
@@ -75,6 +76,8 @@ lib.jllm_q4k_gemv.argtypes = [_P, _P, _P, _I64, _I64, _P, _SZ, _P]
 lib.jllm_q4k_gemv.restype = _ST
 lib.jllm_q4k_gemv_batch.argtypes = [_P, _P, _P, ctypes.c_int, _P, _I64, _P]
 lib.jllm_q4k_gemv_batch.restype = _ST
+lib.jllm_q4k_gemv_rmsnorm_batch.argtypes = [_P, _P, _P, ctypes.c_int, _P, _P, ctypes.c_float, _I64, _P]
+lib.jllm_q4k_gemv_rmsnorm_batch.restype = _ST
 lib.jllm_q4k_gemm.argtypes = [_P, _P, _P, ctypes.c_int, _I64, _I64, _I64, _P, _SZ, _P]
 lib.jllm_q4k_gemm.restype = _ST
 lib.jllm_q4k_gemm_noalloc.argtypes = [_P, _P, _P, ctypes.c_int, _I64, _I64, _I64, _P]
@@ -232,6 +235,32 @@ def jllm_q4k_gemv_batch(ws_q4k, x, Ns, K: int, outs=None, stream=None):
     yp = (ctypes.c_void_p * cnt)(*[o.data_ptr() for o in outs])
     npa = (ctypes.c_int64 * cnt)(*Ns)
     _check(lib.jllm_q4k_gemv_batch(wp, yp, npa, cnt, x.data_ptr(), K, _stream_ptr(stream)), "jllm_q4k_gemv_batch")
+    return outs
+
+
+def jllm_q4k_gemv_rmsnorm_batch(ws_q4k, x, gamma, eps: float, Ns, K: int, outs=None, stream=None):
+    """[y_i[N_i] (fp32) = dequant(W_i) rmsnorm(x)] for up to 8 matrices sharing one fp16 x[K];
+    gamma fp32 [K]; the norm runs in the GEMV's prologue (one launch)."""
+    torch = _torch()
+    ws_q4k, Ns = list(ws_q4k), [int(n) for n in Ns]
+    if not 1 <= len(ws_q4k) <= 8 or len(Ns) != len(ws_q4k):
+        raise ValueError("1 to 8 matrices, one row count each")
+    for i, (w, n) in enumerate(zip(ws_q4k, Ns)):
+        _need(w, torch.uint8, _w_shape(n, K), f"w[{i}]")
+    if x.dim() == 2 and x.shape[0] == 1:
+        x = x.view(K)
+    _need(x, torch.float16, (K,), "x")
+    _need(gamma, torch.float32, (K,), "gamma")
+    if outs is None:
+        outs = [torch.empty((n,), dtype=torch.float32, device=x.device) for n in Ns]
+    for i, (o, n) in enumerate(zip(outs, Ns)):
+        _need(o, torch.float32, (n,), f"out[{i}]")
+    cnt = len(Ns)
+    wp = (ctypes.c_void_p * cnt)(*[w.data_ptr() for w in ws_q4k])
+    yp = (ctypes.c_void_p * cnt)(*[o.data_ptr() for o in outs])
+    npa = (ctypes.c_int64 * cnt)(*Ns)
+    _check(lib.jllm_q4k_gemv_rmsnorm_batch(wp, yp, npa, cnt, x.data_ptr(), gamma.data_ptr(), float(eps), K,
+                                           _stream_ptr(stream)), "jllm_q4k_gemv_rmsnorm_batch")
     return outs
 
 

@@ -163,6 +163,28 @@ jllm_status jllm_q4k_gemv_batch(const void* const* w_q4k, float* const* y, const
                                            (cudaStream_t)stream));
 }
 
+jllm_status jllm_q4k_gemv_rmsnorm_batch(const void* const* w_q4k, float* const* y, const int64_t* N, int count,
+                                        const void* x, const float* gamma, float eps, int64_t K,
+                                        jllm_stream_t stream) {
+  if (!w_q4k || !y || !N || !x || !gamma) return JLLM_ERR_INVALID_ARG;
+  if (count < 1 || count > jllm::kMaxGemvBatch) return JLLM_ERR_INVALID_ARG;
+  if (!(eps >= 0.f) || eps > 1.f) return JLLM_ERR_INVALID_ARG;  // also rejects NaN
+  if (!aligned16(x) || !aligned16(gamma)) return JLLM_ERR_MISALIGNED;
+  int64_t total = 0;
+  for (int i = 0; i < count; ++i) {
+    if (!w_q4k[i] || !y[i]) return JLLM_ERR_INVALID_ARG;
+    jllm_status st = check_shape(1, N[i], K);
+    if (st != JLLM_OK) return st;
+    if (!aligned16(w_q4k[i]) || !aligned16(y[i])) return JLLM_ERR_MISALIGNED;
+    total += N[i];
+  }
+  if (total > kMaxRows) return JLLM_ERR_UNSUPPORTED_SHAPE;
+  jllm_status st = check_device();
+  if (st != JLLM_OK) return st;
+  return from_cuda(jllm::launch_gemv_batch_rmsnorm(w_q4k, reinterpret_cast<void* const*>(y), N, count, x, gamma,
+                                                   eps, K, (cudaStream_t)stream));
+}
+
 jllm_status jllm_q4k_gemm(const void* w_q4k, const void* x, void* y, jllm_dtype y_dt, int64_t M, int64_t N,
                           int64_t K, void* ws, size_t ws_bytes, jllm_stream_t stream) {
   if (!w_q4k || !x || !y) return JLLM_ERR_INVALID_ARG;

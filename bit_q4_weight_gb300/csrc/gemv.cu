@@ -69,6 +69,23 @@ __device__ __forceinline__ void add_halves(float& acc, uint32_t h2) {
       : "r"(h2));
 }
 
+// acc += lo^2 + hi^2 of an fp16 pair (exact products, fp32 sums).
+__device__ __forceinline__ void add_squares(float& acc, uint32_t h2) {
+  asm("{\n .reg .b16 a, b;\n mov.b32 {a, b}, %1;\n"
+      " fma.rn.f32.f16 %0, a, a, %0;\n fma.rn.f32.f16 %0, b, b, %0;\n}"
+      : "+f"(acc)
+      : "r"(h2));
+}
+
+// fp16 pair (x * r * g) of an fp16 pair x, each product rounded in fp32 and
+// the result once to fp16.
+__device__ __forceinline__ uint32_t norm_pair(uint32_t h2, float r, float g0, float g1) {
+  const float a = __fmul_rn(__fmul_rn(half_lo_to_float(h2), r), g0);
+  const float b = __fmul_rn(__fmul_rn(half_hi_to_float(h2), r), g1);
+  const __half2 o = __floats2half2_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&o);
+}
+
 __device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t mask, uint32_t orv) {
   uint32_t r;
   asm("lop3.b32 %0, %1, %2, %3, 0xea;" : "=r"(r) : "r"(a), "r"(mask), "r"(orv));  // (a & b) | c
@@ -194,7 +211,8 @@ template <int R, int W, int KS, bool SWIGLU, int MT>
 __global__ void __launch_bounds__(W * 32, 512 / (W * 32)) q4k_gemv_kernel(const __grid_constant__ GemvBatch batch,
                                                           const uint8_t* __restrict__ W1,
                                                           const __half* __restrict__ x, int NB, int KC,
-                                                          int trigger, int pre, int M, int out_f16) {
+                                                          int trigger, int pre, int M, int out_f16,
+                                                          const float* __restrict__ gamma, float eps) {
   // MT = tokens per launch (M <= MT rows of x, row pitch K); a lane loads each of
   // its weight rows once per block and uses it for every token.
   // KS = K-parts: the 4 groups of a warp form 4/KS row sets x KS K-parts; part
@@ -274,6 +292,11 @@ __global__ void __launch_bounds__(W * 32, 512 / (W * 32)) q4k_gemv_kernel(const 
   // after it.
   if (warp < pre) issue(0);
   if (trigger == 1) pdl_launch_dependents();
+  // gamma is a weight too: pull its lines into L1 before the wait.
+  const bool norm1 = MT == 1 && gamma != nullptr && nchunks == 1 && NB * 8 <= XU * W * 32;
+  if (MT == 1 && gamma != nullptr)
+    for (int sb = threadIdx.x; sb < NB * 8; sb += W * 32)
+      asm volatile("prefetch.global.L1 [%0];" ::"l"(gamma + (size_t)sb * 32));
   pdl_wait();
   if (warp >= pre) issue(0);
   float acc[R][MT];
@@ -289,13 +312,97 @@ __global__ void __launch_bounds__(W * 32, 512 / (W * 32)) q4k_gemv_kernel(const 
     rowp[r] = wtile + (size_t)j * srow;
   }
 
+  // RMSNorm prologue (one token): the CTA sums x^2 over all of K (exact fp16
+  // squares, fp32 sums, a fixed reduction order) for r = 1/sqrt(mean + eps);
+  // the staging below then stores fp16(x * r * gamma) and sums those.
+  // When one pass of the staging loop covers all of x, the squares are summed
+  // from the registers that pass loads instead (no second read of x).
+  float rnorm = 1.f;
+  __shared__ float red[W];
+  if (MT == 1 && gamma != nullptr && !norm1) {
+    float ss = 0.f;
+    for (int sb = threadIdx.x; sb < NB * 8; sb += W * 32) {
+      const __half* src = x + (size_t)sb * 32;
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        const uint4 u = ldg_nc(src + 8 * v);
+        add_squares(ss, u.x);
+        add_squares(ss, u.y);
+        add_squares(ss, u.z);
+        add_squares(ss, u.w);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (lane == 0) red[warp] = ss;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < W; ++w) tot += red[w];
+    rnorm = 1.f / sqrtf(tot / (float)K + eps);
+  }
+
   for (int ch = 0; ch < nchunks; ++ch) {
     const int kb0 = ch * KC, kc = NB - kb0 < KC ? NB - kb0 : KC;
     // Stage this chunk of x (every token row) in the padded layout together with
     // the sums X_j: thread i takes sub-blocks i, i + W*32, ..., XU of them with
     // their loads in flight together.  Token rows m >= M read as zero.
     const int nsb = kc * 8;
-    for (int sb0 = threadIdx.x; sb0 < MT * nsb; sb0 += XU * W * 32) {
+    if (norm1) {
+      // one token, normalised, one pass: load, reduce x^2 over the CTA, scale
+      uint4 u[XU][4];
+      float ss = 0.f;
+#pragma unroll
+      for (int q = 0; q < XU; ++q) {
+        const int sb = threadIdx.x + q * W * 32;
+#pragma unroll
+        for (int v = 0; v < 4; ++v)
+          u[q][v] = sb < nsb ? ldg_nc(x + (size_t)sb * 32 + 8 * v) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int q = 0; q < XU; ++q)
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          add_squares(ss, u[q][v].x);
+          add_squares(ss, u[q][v].y);
+          add_squares(ss, u[q][v].z);
+          add_squares(ss, u[q][v].w);
+        }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      if (lane == 0) red[warp] = ss;
+      __syncthreads();
+      float tot = 0.f;
+#pragma unroll
+      for (int w = 0; w < W; ++w) tot += red[w];
+      rnorm = 1.f / sqrtf(tot / (float)K + eps);
+#pragma unroll
+      for (int q = 0; q < XU; ++q) {
+        const int sb = threadIdx.x + q * W * 32;
+        if (sb < nsb) {
+          const float* g = gamma + (size_t)sb * 32;
+          const int kr = sb >> 3, j = sb & 7;
+          float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const float4 ga = __ldg(reinterpret_cast<const float4*>(g + 8 * v));
+            const float4 gb = __ldg(reinterpret_cast<const float4*>(g + 8 * v + 4));
+            uint4 t = u[q][v];
+            t.x = norm_pair(t.x, rnorm, ga.x, ga.y);
+            t.y = norm_pair(t.y, rnorm, ga.z, ga.w);
+            t.z = norm_pair(t.z, rnorm, gb.x, gb.y);
+            t.w = norm_pair(t.w, rnorm, gb.z, gb.w);
+            xs[x_unit_pos(kr, j >> 1, 4 * (j & 1) + v)] = t;
+            add_halves(s4[v], t.x);
+            add_halves(s4[v], t.y);
+            add_halves(s4[v], t.z);
+            add_halves(s4[v], t.w);
+          }
+          Xs[sb] = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+        }
+      }
+    }
+    for (int sb0 = threadIdx.x; !norm1 && sb0 < MT * nsb; sb0 += XU * W * 32) {
       uint4 u[XU][4];
 #pragma unroll
       for (int q = 0; q < XU; ++q) {
@@ -309,6 +416,24 @@ __global__ void __launch_bounds__(W * 32, 512 / (W * 32)) q4k_gemv_kernel(const 
           } else {
 #pragma unroll
             for (int v = 0; v < 4; ++v) u[q][v] = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+      }
+      if (MT == 1 && gamma != nullptr) {
+#pragma unroll
+        for (int q = 0; q < XU; ++q) {
+          const int sb = sb0 + q * W * 32;
+          if (sb < nsb) {
+            const float* g = gamma + (size_t)(kb0 + (sb >> 3)) * QK + 32 * (sb & 7);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              const float4 ga = __ldg(reinterpret_cast<const float4*>(g + 8 * v));
+              const float4 gb = __ldg(reinterpret_cast<const float4*>(g + 8 * v + 4));
+              u[q][v].x = norm_pair(u[q][v].x, rnorm, ga.x, ga.y);
+              u[q][v].y = norm_pair(u[q][v].y, rnorm, ga.z, ga.w);
+              u[q][v].z = norm_pair(u[q][v].z, rnorm, gb.x, gb.y);
+              u[q][v].w = norm_pair(u[q][v].w, rnorm, gb.z, gb.w);
+            }
           }
         }
       }
@@ -461,6 +586,8 @@ struct GemvJob {
   int64_t K;
   int M;           // tokens (rows of x), 1..kMaxGemvTokens
   int out_f16;
+  const float* gamma = nullptr;  // RMSNorm weight [K] (one token only), else nullptr
+  float eps = 0.f;
 };
 
 template <int R, int W, int KS, bool SWIGLU, int MT>
@@ -499,7 +626,7 @@ cudaError_t launch_gemv_cfg(const GemvJob& job, cudaStream_t stream, bool pdl, i
   cfg.numAttrs = pdl ? 1 : 0;
   const int pre = (W * pre_pct + 99) / 100;
   return cudaLaunchKernelEx(&cfg, kern, b, static_cast<const uint8_t*>(job.w1), static_cast<const __half*>(job.x),
-                            NB, KC, trigger, pre, job.M, job.out_f16);
+                            NB, KC, trigger, pre, job.M, job.out_f16, job.gamma, job.eps);
 }
 
 // The first configuration whose whole-row weight tile fits the tile cap and
@@ -545,7 +672,7 @@ cudaError_t run_gemv(const GemvJob& job, cudaStream_t stream) {
   int64_t rows = 0;
   for (int i = 0; i < job.count; ++i) rows += job.n[i];
   if (job.M > 1) {
-    if (job.w1 != nullptr || job.count != 1) return cudaErrorInvalidValue;
+    if (job.w1 != nullptr || job.count != 1 || job.gamma != nullptr) return cudaErrorInvalidValue;
     if (job.M <= 2) return run_gemv_multi<2>(job, stream, pdl, kn, rows, NB, dev.sm_count);
     if (job.M <= 4) return run_gemv_multi<4>(job, stream, pdl, kn, rows, NB, dev.sm_count);
     if (job.M <= 8) return run_gemv_multi<8>(job, stream, pdl, kn, rows, NB, dev.sm_count);
@@ -591,6 +718,15 @@ cudaError_t launch_gemv_batch(const void* const* w, void* const* y, const int64_
                               int64_t K, cudaStream_t stream) {
   if (count < 1 || count > kMaxGemvBatch) return cudaErrorInvalidValue;
   return run_gemv(GemvJob{w, y, N, count, nullptr, x, K, 1, 0}, stream);
+}
+
+cudaError_t launch_gemv_batch_rmsnorm(const void* const* w, void* const* y, const int64_t* N, int count,
+                                      const void* x, const float* gamma, float eps, int64_t K, cudaStream_t stream) {
+  if (count < 1 || count > kMaxGemvBatch || gamma == nullptr) return cudaErrorInvalidValue;
+  GemvJob job{w, y, N, count, nullptr, x, K, 1, 0};
+  job.gamma = gamma;
+  job.eps = eps;
+  return run_gemv(job, stream);
 }
 
 cudaError_t read_clear_gemv_error(uint32_t* bits) {

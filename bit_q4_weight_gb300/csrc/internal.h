@@ -35,6 +35,11 @@ constexpr int kMaxGemvBatch = 8;
 cudaError_t launch_gemv_batch(const void* const* w, void* const* y, const int64_t* N, int count, const void* x,
                               int64_t K, cudaStream_t s);
 
+// launch_gemv_batch on x normalised in the prologue:
+// xn = fp16(x * gamma / sqrt(mean(x^2) + eps)), gamma fp32 [K], one token.
+cudaError_t launch_gemv_batch_rmsnorm(const void* const* w, void* const* y, const int64_t* N, int count,
+                                      const void* x, const float* gamma, float eps, int64_t K, cudaStream_t s);
+
 // TMA + tcgen05 GEMM for any M >= 1.  w1 != nullptr selects the SwiGLU
 // epilogue (y = fp16 h).  ws (nullptr allowed) of at least
 // gemm_workspace_bytes() zero-initialised bytes enables the stream-K split.

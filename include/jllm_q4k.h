@@ -125,6 +125,31 @@ jllm_status jllm_q4k_gemv_batch(const void* const* w_q4k, float* const* y, const
                                 const void* x, int64_t K, jllm_stream_t stream);
 
 /*
+ * jllm_q4k_gemv_rmsnorm_batch -- jllm_q4k_gemv_batch on the RMS-normalised x:
+ *   xn[k] = fp16( x[k] * r * gamma[k] ),  r = 1 / sqrt(sum_k x[k]^2 / K + eps)
+ *   y[i][n] = sum_k xn[k] * w_i[n,k]
+ * The RMSNorm of the README's "fused RMSNorm + RoPE + SwiGLU" kernel (At a
+ * glance, Kernels bullet), fused into the prologue of the decode GEMV so that
+ * a decoder layer's q/k/v (and gate/up) launch reads the residual stream
+ * directly.  The pages print no formula; this is the standard RMSNorm.
+ *   x     : [K] fp16, shared; gamma: [K] fp32 (16-byte aligned); eps in [0, 1]
+ *   w_q4k, y, N, count: as jllm_q4k_gemv_batch
+ * gamma, like the weights, is read before the wait on the previous kernel in
+ * the stream (see the PDL paragraph above): it must not be written by that
+ * kernel.
+ * Every CTA forms r itself (fp32 sum of exact fp16 squares in a fixed order,
+ * then 1/sqrt), so r is the same for all outputs.  The normalised x is
+ * rounded to fp16 (the GEMV's input type) before the products; y is within
+ * the matmul bound of the exact xn with one extra 2^-11 relative term for
+ * that rounding, which the bound covers.
+ * Errors: INVALID_ARG (also count outside 1..8, eps outside [0, 1] or NaN),
+ *         UNSUPPORTED_SHAPE, MISALIGNED, CUDA.
+ */
+jllm_status jllm_q4k_gemv_rmsnorm_batch(const void* const* w_q4k, float* const* y, const int64_t* N,
+                                        int count, const void* x, const float* gamma, float eps,
+                                        int64_t K, jllm_stream_t stream);
+
+/*
  * jllm_q4k_gemm -- Y[M,N] = X[M,K] * dequant(W)^T for any M >= 1.
  * (the README's "tensor-core MMQ Q4_K prefill" for M above the GEMV
  *  threshold, the GEMV kernel at or below it)

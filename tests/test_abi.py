@@ -145,6 +145,25 @@ def test_gemm_batch_argument_errors(q):
     assert call(w4, A, y4, 0, 64, n4, 256, 2, None, 0, None) == 1  # N < 1
 
 
+def test_gemv_rmsnorm_batch_argument_errors(q):
+    import ctypes
+
+    A = ALIGNED
+    P = ctypes.c_void_p
+    w = (P * 2)(A, A)
+    y = (P * 2)(A, A)
+    n = (ctypes.c_int64 * 2)(4, 8)
+    call = q.lib.jllm_q4k_gemv_rmsnorm_batch
+    assert call(w, y, n, 2, A, None, 1e-6, 256, None) == 1  # no gamma
+    assert call(w, y, n, 0, A, A, 1e-6, 256, None) == 1  # count 0
+    assert call(w, y, n, 9, A, A, 1e-6, 256, None) == 1  # count above 8
+    assert call(w, y, n, 2, A, A, -1.0, 256, None) == 1  # eps < 0
+    assert call(w, y, n, 2, A, A, float("nan"), 256, None) == 1  # eps NaN
+    assert call(w, y, n, 2, A, A + 4, 1e-6, 256, None) == 3  # gamma misaligned
+    assert call(w, y, n, 2, A + 2, A, 1e-6, 256, None) == 3  # x misaligned
+    assert call(w, y, n, 2, A, A, 1e-6, 300, None) == 2  # K % 256
+
+
 def _no_cuda():
     try:
         import torch
