@@ -207,7 +207,7 @@ struct GemvBatch {
 // Per chunk, warp w's rows arrive by bulk copy on the warp's own mbarrier --
 // a single copy when the chunk is the whole row, since the warp's rows are
 // then contiguous in W -- and each warp starts as soon as its rows land.
-template <int R, int W, int KS, bool SWIGLU, int MT>
+template <int R, int W, int KS, bool SWIGLU, int MT, bool NORM>
 __global__ void __launch_bounds__(W * 32, 512 / (W * 32)) q4k_gemv_kernel(const __grid_constant__ GemvBatch batch,
                                                           const uint8_t* __restrict__ W1,
                                                           const __half* __restrict__ x, int NB, int KC,
@@ -293,8 +293,8 @@ __global__ void __launch_bounds__(W * 32, 512 / (W * 32)) q4k_gemv_kernel(const 
   if (warp < pre) issue(0);
   if (trigger == 1) pdl_launch_dependents();
   // gamma is a weight too: pull its lines into L1 before the wait.
-  const bool norm1 = MT == 1 && gamma != nullptr && nchunks == 1 && NB * 8 <= XU * W * 32;
-  if (MT == 1 && gamma != nullptr)
+  const bool norm1 = NORM && nchunks == 1 && NB * 8 <= XU * W * 32;
+  if (NORM)
     for (int sb = threadIdx.x; sb < NB * 8; sb += W * 32)
       asm volatile("prefetch.global.L1 [%0];" ::"l"(gamma + (size_t)sb * 32));
   pdl_wait();
@@ -319,7 +319,7 @@ __global__ void __launch_bounds__(W * 32, 512 / (W * 32)) q4k_gemv_kernel(const 
   // from the registers that pass loads instead (no second read of x).
   float rnorm = 1.f;
   __shared__ float red[W];
-  if (MT == 1 && gamma != nullptr && !norm1) {
+  if (NORM && !norm1) {
     float ss = 0.f;
     for (int sb = threadIdx.x; sb < NB * 8; sb += W * 32) {
       const __half* src = x + (size_t)sb * 32;
@@ -419,7 +419,7 @@ __global__ void __launch_bounds__(W * 32, 512 / (W * 32)) q4k_gemv_kernel(const 
           }
         }
       }
-      if (MT == 1 && gamma != nullptr) {
+      if (NORM) {
 #pragma unroll
         for (int q = 0; q < XU; ++q) {
           const int sb = sb0 + q * W * 32;
@@ -590,7 +590,7 @@ struct GemvJob {
   float eps = 0.f;
 };
 
-template <int R, int W, int KS, bool SWIGLU, int MT>
+template <int R, int W, int KS, bool SWIGLU, int MT, bool NORM = false>
 cudaError_t launch_gemv_cfg(const GemvJob& job, cudaStream_t stream, bool pdl, int trigger, int pre_pct) {
   const int NB = (int)(job.K / QK);
   constexpr int RP = SWIGLU ? R / 2 : R;
@@ -609,7 +609,8 @@ cudaError_t launch_gemv_cfg(const GemvJob& job, cudaStream_t stream, bool pdl, i
   b.count = job.count;
   if (grid > INT32_MAX) return cudaErrorInvalidValue;
   const size_t smem = gemv_smem_bytes<R, W, KS, MT>(KC);
-  auto kern = q4k_gemv_kernel<R, W, KS, SWIGLU, MT>;
+  static_assert(!NORM || (MT == 1 && !SWIGLU), "the RMSNorm prologue is one-token, single-output");
+  auto kern = q4k_gemv_kernel<R, W, KS, SWIGLU, MT, NORM>;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -679,13 +680,23 @@ cudaError_t run_gemv(const GemvJob& job, cudaStream_t stream) {
     return cudaErrorInvalidValue;
   }
   if (job.w1 == nullptr) {
-    if (kn.R) {
+    if (kn.R && job.gamma == nullptr) {
 #define X(R_, W_, KS_) \
   if (kn.R == R_ && kn.W == W_ && kn.KS == KS_) return launch_gemv_cfg<R_, W_, KS_, false, 1>(job, stream, pdl, kn.trigger, kn.pre_pct);
       JLLM_GEMV_CFGS(X)
 #undef X
     }
     static const Cfg cfgs[] = {{2, 8, 1}, {2, 4, 1}, {1, 4, 1}, {1, 4, 2}, {1, 4, 4}, {1, 2, 4}};
+    if (job.gamma != nullptr) {  // RMSNorm prologue: its own instantiations
+      switch (pick<false>(cfgs, 6, rows, NB, dev.sm_count, kn.ctas_per_sm)) {
+        case 0: return launch_gemv_cfg<2, 8, 1, false, 1, true>(job, stream, pdl, kn.trigger, kn.pre_pct);
+        case 1: return launch_gemv_cfg<2, 4, 1, false, 1, true>(job, stream, pdl, kn.trigger, kn.pre_pct);
+        case 2: return launch_gemv_cfg<1, 4, 1, false, 1, true>(job, stream, pdl, kn.trigger, kn.pre_pct);
+        case 3: return launch_gemv_cfg<1, 4, 2, false, 1, true>(job, stream, pdl, kn.trigger, kn.pre_pct);
+        case 4: return launch_gemv_cfg<1, 4, 4, false, 1, true>(job, stream, pdl, kn.trigger, kn.pre_pct);
+        default: return launch_gemv_cfg<1, 2, 4, false, 1, true>(job, stream, pdl, kn.trigger, kn.pre_pct);
+      }
+    }
     switch (pick<false>(cfgs, 6, rows, NB, dev.sm_count, kn.ctas_per_sm)) {
       case 0: return launch_gemv_cfg<2, 8, 1, false, 1>(job, stream, pdl, kn.trigger, kn.pre_pct);
       case 1: return launch_gemv_cfg<2, 4, 1, false, 1>(job, stream, pdl, kn.trigger, kn.pre_pct);
