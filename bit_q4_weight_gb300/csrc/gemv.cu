@@ -686,13 +686,13 @@ cudaError_t run_gemv(const GemvJob& job, cudaStream_t stream) {
       JLLM_GEMV_CFGS(X)
 #undef X
     }
-    static const Cfg cfgs[] = {{2, 8, 1}, {2, 4, 1}, {1, 4, 1}, {1, 4, 2}, {1, 4, 4}, {1, 2, 4}};
+    static const Cfg cfgs[] = {{2, 8, 1}, {2, 4, 1}, {1, 4, 1}, {2, 4, 4}, {1, 4, 4}, {1, 2, 4}};
     if (job.gamma != nullptr) {  // RMSNorm prologue: its own instantiations
       switch (pick<false>(cfgs, 6, rows, NB, dev.sm_count, kn.ctas_per_sm)) {
         case 0: return launch_gemv_cfg<2, 8, 1, false, 1, true>(job, stream, pdl, kn.trigger, kn.pre_pct);
         case 1: return launch_gemv_cfg<2, 4, 1, false, 1, true>(job, stream, pdl, kn.trigger, kn.pre_pct);
         case 2: return launch_gemv_cfg<1, 4, 1, false, 1, true>(job, stream, pdl, kn.trigger, kn.pre_pct);
-        case 3: return launch_gemv_cfg<1, 4, 2, false, 1, true>(job, stream, pdl, kn.trigger, kn.pre_pct);
+        case 3: return launch_gemv_cfg<2, 4, 4, false, 1, true>(job, stream, pdl, kn.trigger, kn.pre_pct);
         case 4: return launch_gemv_cfg<1, 4, 4, false, 1, true>(job, stream, pdl, kn.trigger, kn.pre_pct);
         default: return launch_gemv_cfg<1, 2, 4, false, 1, true>(job, stream, pdl, kn.trigger, kn.pre_pct);
       }
@@ -701,7 +701,7 @@ cudaError_t run_gemv(const GemvJob& job, cudaStream_t stream) {
       case 0: return launch_gemv_cfg<2, 8, 1, false, 1>(job, stream, pdl, kn.trigger, kn.pre_pct);
       case 1: return launch_gemv_cfg<2, 4, 1, false, 1>(job, stream, pdl, kn.trigger, kn.pre_pct);
       case 2: return launch_gemv_cfg<1, 4, 1, false, 1>(job, stream, pdl, kn.trigger, kn.pre_pct);
-      case 3: return launch_gemv_cfg<1, 4, 2, false, 1>(job, stream, pdl, kn.trigger, kn.pre_pct);
+      case 3: return launch_gemv_cfg<2, 4, 4, false, 1>(job, stream, pdl, kn.trigger, kn.pre_pct);
       case 4: return launch_gemv_cfg<1, 4, 4, false, 1>(job, stream, pdl, kn.trigger, kn.pre_pct);
       default: return launch_gemv_cfg<1, 2, 4, false, 1>(job, stream, pdl, kn.trigger, kn.pre_pct);
     }
