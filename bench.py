@@ -205,6 +205,16 @@ def run_plan(q, plan):
             q.jllm_q4k_gemv_batch(ws, x, ns, K, outs=ys)
 
 
+def max_over_ranks(torch, dist, t, world, device=None):
+    """Seconds maxed over the ranks: the slowest replica sets the job's time (a collective
+    over the timing only; the data path has none)."""
+    if world <= 1:
+        return t
+    tt = torch.tensor([float(t)], dtype=torch.float64, device=device)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt.item())
+
+
 def time_graph(torch, graph, stream, steps, warmup, clk=None):
     """Seconds per replay, CUDA events recorded on the stream the graph is launched on."""
     with torch.cuda.stream(stream):
@@ -258,25 +268,29 @@ def run_ours(args):
         torch.cuda.synchronize()
         return g
 
-    g = capture(plan)
-    if world > 1:
-        dist.barrier()
-    with ClockSampler(local) as clk:
+    def sync_ranks():
         torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+
+    def tmax(t):
+        return max_over_ranks(torch, dist, t, world, dev)
+
+    g = capture(plan)
+    sync_ranks()
+    with ClockSampler(local) as clk:
         t_step = time_graph(torch, g, stream, args.steps, args.warmup, clk)
     clocks = clk.summary()
-    t_max = t_step
-    if world > 1:
-        tt = torch.tensor([t_step], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_max = float(tt.item())
+    sync_ranks()
+    t_max = tmax(t_step)
     value = total_bytes * world / t_max / 1e9
     del g
 
     # the same weights, seven single-matrix launches per layer
     plan7 = decode_plan(W, XG, Y, meta, batched=False)
     g7 = capture(plan7)
-    t7 = time_graph(torch, g7, stream, args.steps, args.warmup)
+    sync_ranks()
+    t7 = tmax(time_graph(torch, g7, stream, args.steps, args.warmup))
     del g7
 
     # the same batched sweep with the RMSNorm prologue on the q/k/v and gate/up launches
@@ -305,7 +319,8 @@ def run_ours(args):
     with torch.cuda.graph(gn, stream=stream):
         run_plan_norm()
     torch.cuda.synchronize()
-    tn = time_graph(torch, gn, stream, args.steps, args.warmup)
+    sync_ranks()
+    tn = tmax(time_graph(torch, gn, stream, args.steps, args.warmup))
     del gn
 
     # end to end: host->device copy of every activation, the sweep, device->host of every output
@@ -333,11 +348,7 @@ def run_ours(args):
     t0 = time.perf_counter()
     for _ in range(args.steps):
         e2e_step()
-    t_e2e = (time.perf_counter() - t0) / args.steps
-    if world > 1:
-        tt = torch.tensor([t_e2e], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_e2e = float(tt.item())
+    t_e2e = tmax((time.perf_counter() - t0) / args.steps)
     e2e = {"value": round(total_bytes * world / t_e2e / 1e9, 2), "unit": "GB/s",
            "h2d_bytes_per_step": int(xs_host.numel() * 2), "d2h_bytes_per_step": int(ys_host.numel() * 4)}
     del ge
@@ -371,7 +382,7 @@ def run_ours(args):
     ffn = None
     short = None
     if not args.no_prefill:
-        prefill = run_prefill(torch, q, W, meta, dev, stream, args, world)
+        prefill = run_prefill(torch, q, W, meta, dev, stream, args, world, tmax=tmax, sync=sync_ranks)
         if rank == 0:
             ffn = run_ffn_lmhead(torch, q, W, dev, stream, args)
             short = {f"M{m}": run_prefill(torch, q, W, meta, dev, stream, args, world, M=m, short=True)
@@ -522,7 +533,7 @@ def run_ffn_lmhead(torch, q, W, dev, stream, args):
     return out
 
 
-def run_prefill(torch, q, W, meta, dev, stream, args, world, M=M_PREFILL, short=False):
+def run_prefill(torch, q, W, meta, dev, stream, args, world, M=M_PREFILL, short=False, tmax=None, sync=None):
     """M = 2048 tcgen05 GEMMs over the same resident weights, fp16 out.  The value is
     the layer's data flow in four launches (q/k/v and gate/up each one batched GEMM
     on their shared X, then o, then down); the seven-call sweep is timed beside it.
@@ -572,9 +583,14 @@ def run_prefill(torch, q, W, meta, dev, stream, args, world, M=M_PREFILL, short=
                 "tflops": round(flops / t / 1e12, 2), "launches_per_step": layers * len(GROUPS),
                 "seven_call": {"us_per_step": round(t7 * 1e6, 1), "weight_gbs": round(wb / t7 / 1e9, 1),
                                "tflops": round(flops / t7 / 1e12, 2)}}
+    tmax = tmax or (lambda t: t)
+    if sync:
+        sync()
     with ClockSampler(int(os.environ.get("LOCAL_RANK", "0"))) as clk:
-        t = timed(sweep_batched, clk)
-    t7 = timed(sweep7)
+        t = tmax(timed(sweep_batched, clk))
+    if sync:
+        sync()
+    t7 = tmax(timed(sweep7))
     peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
         os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
     peak = peaks.get("bf16_tflops_sustained", 1700.0)
