@@ -359,6 +359,12 @@ __global__ void __launch_bounds__(W * 32, 512 / (W * 32)) q4k_gemv_kernel(const 
         for (int v = 0; v < 4; ++v)
           u[q][v] = sb < nsb ? ldg_nc(x + (size_t)sb * 32 + 8 * v) : make_uint4(0u, 0u, 0u, 0u);
       }
+      // gamma of the first sub-block, in flight together with x
+      float4 g0[8];
+#pragma unroll
+      for (int v = 0; v < 8; ++v)
+        g0[v] = (int)threadIdx.x < nsb ? __ldg(reinterpret_cast<const float4*>(gamma + (size_t)threadIdx.x * 32) + v)
+                                       : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int q = 0; q < XU; ++q)
 #pragma unroll
@@ -385,8 +391,8 @@ __global__ void __launch_bounds__(W * 32, 512 / (W * 32)) q4k_gemv_kernel(const 
           float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
-            const float4 ga = __ldg(reinterpret_cast<const float4*>(g + 8 * v));
-            const float4 gb = __ldg(reinterpret_cast<const float4*>(g + 8 * v + 4));
+            const float4 ga = q == 0 ? g0[2 * v] : __ldg(reinterpret_cast<const float4*>(g + 8 * v));
+            const float4 gb = q == 0 ? g0[2 * v + 1] : __ldg(reinterpret_cast<const float4*>(g + 8 * v + 4));
             uint4 t = u[q][v];
             t.x = norm_pair(t.x, rnorm, ga.x, ga.y);
             t.y = norm_pair(t.y, rnorm, ga.z, ga.w);
