@@ -7,6 +7,7 @@ nothing but the NVIDIA driver at run time.
 from __future__ import annotations
 
 import concurrent.futures as cf
+import fcntl
 import os
 import shutil
 import subprocess
@@ -37,12 +38,26 @@ def _newest_input() -> float:
     return max(os.path.getmtime(f) for f in files)
 
 
+def _up_to_date() -> bool:
+    return os.path.exists(LIB) and os.path.getmtime(LIB) >= _newest_input()
+
+
 def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None) -> str:
-    """Compile the library if it is missing or older than its sources; return its path."""
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _newest_input():
+    """Compile the library if it is missing or older than its sources; return its path.
+    Processes that build at the same time (the ranks of one job) take turns on a lock
+    file, and a process that waited finds the library already built."""
+    if not force and _up_to_date():
         return LIB
-    nvcc = _nvcc()
     os.makedirs(BUILD, exist_ok=True)
+    with open(os.path.join(BUILD, ".lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        if not force and _up_to_date():
+            return LIB
+        return _build_locked(verbose, extra)
+
+
+def _build_locked(verbose: bool, extra: list[str] | None) -> str:
+    nvcc = _nvcc()
     flags = ARCH + CFLAGS + (extra or [])
 
     def compile_one(src: str) -> str:

@@ -91,3 +91,27 @@ def test_reference_arm_rank0_prints_one_line(monkeypatch):
     line = json.loads(lines[0])
     assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_profiled_traffic_follows_the_source_hash(tmp_path, monkeypatch):
+    """roofline.traffic is read from a profiles/ record only while the kernel's sources
+    still hash to the value recorded with the counters."""
+    import hashlib
+
+    sys.path.insert(0, ROOT)
+    import bench
+
+    csrc = tmp_path / "bit_q4_weight_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (csrc / "k.cu").write_text("kernel v1\n")
+    (csrc / "common.cuh").write_text("helpers\n")
+    h = hashlib.sha256(b"kernel v1\n" + b"helpers\n").hexdigest()[:16]
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    (prof / "t.md").write_text(f"<!-- traffic kernel=k_kernel sources=k.cu,common.cuh sha256_16={h} "
+                               "bytes_per_launch=12345 -->\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.profiled_traffic("k_kernel") == 12345
+    assert bench.profiled_traffic("other_kernel") is None
+    (csrc / "k.cu").write_text("kernel v2\n")  # the kernel changed since the capture
+    assert bench.profiled_traffic("k_kernel") is None
