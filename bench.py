@@ -414,7 +414,8 @@ def run_ours(args):
                          "unit": "GB/s", "frac": round(total_bytes / t_step / 1e9 / hbm_peak, 4),
                          "traffic": profiled_traffic("q4k_gemv_kernel"), "peak_source": peak_note,
                          "bytes_per_launch": round(total_bytes / n_launch),
-                         "kernel": "q4k_gemv_kernel", "avg_launch_us": round(t_step / n_launch * 1e6, 3)},
+                         "kernel": "q4k_gemv_kernel", "avg_launch_us": round(t_step / n_launch * 1e6, 3),
+                         "frac_of_nominal_7900": round(total_bytes / t_step / 1e9 / 7900.0, 4)},
             "e2e": e2e,
             "decode_7call": {"value": round(total_bytes * world / t7 / 1e9, 2), "unit": "GB/s",
                              "ms_per_step": round(t7 * 1e3, 4), "launches_per_step": len(plan7)},

@@ -6,8 +6,8 @@
  * the two kernels the genie-ai-runtime README lists under "At a glance"
  * (Kernels bullet) and "Project layout" (src/kernels/): the "INT4
  * dequant-fused GEMV" used for decode (M = 1) and the "tensor-core MMQ Q4_K
- * prefill" used for prompts (M = prompt tokens); and of the SwiGLU part of its
- * "fused RMSNorm + RoPE + SwiGLU" kernel.  The pages say the runtime loads
+ * prefill" used for prompts (M = prompt tokens); and of the SwiGLU and RMSNorm
+ * parts of its "fused RMSNorm + RoPE + SwiGLU" kernel.  The pages say the runtime loads
  * GGUF Q4_K_M models ("At a glance", Models bullet) but print neither the
  * block layout nor any kernel interface; both are defined here.
  *
