@@ -714,6 +714,13 @@ cudaError_t launch_tc_common(const void* const* w, const void* w1, const int64_t
   if (kn.bn >= 16 && kn.bn <= bn_cap && kn.bn % 16 == 0) bn_cap = kn.bn;
   int BN = (int)((M + 15) / 16 * 16);
   if (BN > bn_cap) BN = bn_cap;
+  // A mid-size M (one token tile, more than half the cap) over few weight-row
+  // tiles: two token tiles of half the size put twice the CTAs to work while
+  // they still fit in one wave (each weight tile is then dequantised twice).
+  int64_t n_tiles = 0;
+  for (int b = 0; b < count; ++b) n_tiles += Ns[b] > 0 ? (Ns[b] + TILE_N - 1) / TILE_N : 0;
+  if (kn.bn == 0 && M > bn_cap / 2 && M <= bn_cap && 2 * n_tiles <= dev.sm_count)
+    BN = (int)(((M + 1) / 2 + 15) / 16 * 16);
 
   GemmParams p = {};
   p.M = (int)M;
