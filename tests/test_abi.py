@@ -68,6 +68,8 @@ ALIGNED = 1 << 20  # a non-null, 16-byte-aligned fake address (never dereference
         ((ALIGNED, ALIGNED, ALIGNED, 0, 4, 128, 300, None, 0, None), 2),    # K % 256
         ((ALIGNED, ALIGNED, ALIGNED, 0, 4, 128, 0, None, 0, None), 2),      # K = 0
         ((ALIGNED, ALIGNED, ALIGNED, 0, 4, 128, 1 << 40, None, 0, None), 2),  # K too large
+        ((ALIGNED, ALIGNED, ALIGNED, 0, 4, (1 << 30) + 1, 256, None, 0, None), 2),  # N beyond the index range
+        ((ALIGNED, ALIGNED, ALIGNED, 0, (1 << 30) + 1, 128, 256, None, 0, None), 2),  # M beyond the index range
         ((ALIGNED, ALIGNED, ALIGNED, 7, 4, 128, 256, None, 0, None), 4),    # dtype
         ((ALIGNED + 8, ALIGNED, ALIGNED, 0, 4, 128, 256, None, 0, None), 3),  # W misaligned
         ((ALIGNED, ALIGNED + 2, ALIGNED, 0, 4, 128, 256, None, 0, None), 3),  # X misaligned
