@@ -23,12 +23,18 @@
 //    is used, into a padded shared layout whose 144-byte chunk stride puts
 //    the eight lanes of a group in eight different bank groups; the
 //    32-element sums X_j of every sub-block are formed on the way.
-//  * Math.  Each code byte becomes two fp16 values 1024+q (low nibble) and
-//    1024+16q (high nibble) with one LOP3 per pair; products with x are
-//    accumulated in fp32 by the mixed-precision fma.rn.f32.f16 (exact
-//    products).  Per sub-block j the offset is removed with the x sums:
-//        sum_i w_i x_i = d*sc_j * (A_j - 1024*X_j) / (1 or 16) - dmin*m_j * X_j
+//  * Math.  Each code byte becomes two fp16 values by one AND per pair: the
+//    low nibble left in place is the fp16 subnormal q*2^-24, the high nibble
+//    left at bits 4..7 is 16q*2^-24.  Both are exact, with no offset to
+//    remove afterwards.  Their products with x are accumulated in fp32 by the
+//    mixed-precision fma.rn.f32.f16 (exact products), so per sub-block j
+//        A_j = 2^-24 * sum_i q_i x_i        (or 16 * that for high nibbles)
+//    and the staged x sums X_j are kept scaled by 2^-24 as well:
+//        sum_i w_i x_i = 2^24 * ( d*sc_j * A_j (/16) - dmin*m_j * X_j*2^-24 )
 //    which is the block value d*sc_j*q - dmin*m_j summed against x.  The
+//    power-of-two scalings are exact; the row total is multiplied by 2^24
+//    once at the end.  A code of 0 contributes an exact 0, so a sub-block
+//    whose weights are all zero adds nothing, whatever its scale.  The
 //    6-bit sc_j and m_j of a lane's two sub-blocks come out of the packed
 //    bytes as one fp16 pair each (byte permute, masks, 1024 offset), and
 //    d*sc_j, dmin*m_j are exact fp16 x fp16 products in fp32: no integer
@@ -148,20 +154,20 @@ __device__ __forceinline__ void scale_acc(float& acc, uint32_t dd, uint32_t sc2,
       : "r"(dd), "r"(sc2), "r"(nm2), "f"(p0), "f"(p1), "f"(x0), "f"(x1), "f"(0.f));
 }
 
-// acc += partial dot product of one lane's chunk (64 weights) of one block row.
+// acc += 2^-24 * (partial dot product of one lane's chunk (64 weights) of one
+// block row); Xlo, Xhi are the chunk's two x sums times 2^-24.
 __device__ __forceinline__ void chunk_dot(float& acc, const RowData& d, const uint4 (&xv)[8], float Xlo, float Xhi,
                                           const LaneDec& L) {
   const uint32_t qw[8] = {d.q0.x, d.q0.y, d.q0.z, d.q0.w, d.q1.x, d.q1.y, d.q1.z, d.q1.w};
-  // The 1024 offset of the codes is taken out up front: A_j starts at -1024 X_j.
-  float alo0 = -1024.f * Xlo, alo1 = 0.f, ahi0 = -1024.f * Xhi, ahi1 = 0.f;
+  float alo0 = 0.f, alo1 = 0.f, ahi0 = 0.f, ahi1 = 0.f;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const uint32_t w = qw[i];
     const uint32_t w8 = w >> 8;
-    const uint32_t l02 = lop3_and_or(w, 0x000F000Fu, 0x64006400u);   // 1024+q  (bytes 0,2 low)
-    const uint32_t l13 = lop3_and_or(w8, 0x000F000Fu, 0x64006400u);  // 1024+q  (bytes 1,3 low)
-    const uint32_t h02 = lop3_and_or(w, 0x00F000F0u, 0x64006400u);   // 1024+16q (bytes 0,2 high)
-    const uint32_t h13 = lop3_and_or(w8, 0x00F000F0u, 0x64006400u);  // 1024+16q (bytes 1,3 high)
+    const uint32_t l02 = w & 0x000F000Fu;   // q*2^-24   (bytes 0,2 low nibbles, fp16 subnormals)
+    const uint32_t l13 = w8 & 0x000F000Fu;  // q*2^-24   (bytes 1,3 low)
+    const uint32_t h02 = w & 0x00F000F0u;   // 16q*2^-24 (bytes 0,2 high)
+    const uint32_t h13 = w8 & 0x00F000F0u;  // 16q*2^-24 (bytes 1,3 high)
     const uint4 xl = xv[i >> 1];
     const uint4 xh = xv[4 + (i >> 1)];
     const uint32_t xla = (i & 1) ? xl.z : xl.x, xlb = (i & 1) ? xl.w : xl.y;
@@ -185,10 +191,14 @@ __device__ __forceinline__ void chunk_dot(float& acc, const RowData& d, const ui
   mw = lop3_and_or(pz >> 2, L.mc, mw);
   const uint32_t sc2 = hfma2_bits(scw, 0x2C003C00u, 0xD400E400u);  // * (1, 1/16) + (-1024, -64)
   const uint32_t nm2 = hfma2_bits(mw, 0xBC00BC00u, 0x64006400u);   // * (-1, -1) + (1024, 1024)
-  //   sum_i w_i x_i = d*sc_lo * (A_lo - 1024 X_lo) + d*sc_hi/16 * (A_hi - 1024 X_hi)
-  //                   - dmin*m_lo * X_lo - dmin*m_hi * X_hi
+  //   2^-24 sum_i w_i x_i = d*sc_lo * A_lo + d*sc_hi/16 * A_hi
+  //                         - dmin*m_lo * X_lo - dmin*m_hi * X_hi      (A, X scaled by 2^-24)
   scale_acc(acc, d.h.x, sc2, nm2, alo0 + alo1, ahi0 + ahi1, Xlo, Xhi);
 }
+
+// Exact power-of-two scalings of the subnormal-code dot product.
+constexpr float kTwoM24 = 5.9604644775390625e-8f;  // 2^-24
+constexpr float kTwo24 = 16777216.0f;              // 2^24
 
 __device__ uint32_t g_gemv_error;
 constexpr uint64_t GEMV_WAIT_LIMIT_NS = 2000000000ull;  // 2 s
@@ -404,7 +414,7 @@ __global__ void __launch_bounds__(W * 32, 512 / (W * 32)) q4k_gemv_kernel(const 
             add_halves(s4[v], t.z);
             add_halves(s4[v], t.w);
           }
-          Xs[sb] = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+          Xs[sb] = ((s4[0] + s4[1]) + (s4[2] + s4[3])) * kTwoM24;
         }
       }
     }
@@ -459,7 +469,7 @@ __global__ void __launch_bounds__(W * 32, 512 / (W * 32)) q4k_gemv_kernel(const 
             add_halves(s4[v], u[q][v].z);
             add_halves(s4[v], u[q][v].w);
           }
-          Xs[(size_t)m * KC * 8 + sl] = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+          Xs[(size_t)m * KC * 8 + sl] = ((s4[0] + s4[1]) + (s4[2] + s4[3])) * kTwoM24;
         }
       }
     }
@@ -509,7 +519,7 @@ __global__ void __launch_bounds__(W * 32, 512 / (W * 32)) q4k_gemv_kernel(const 
       v += __shfl_xor_sync(0xffffffffu, v, 4);
       if (KS >= 2) v += __shfl_xor_sync(0xffffffffu, v, 8);
       if (KS == 4) v += __shfl_xor_sync(0xffffffffu, v, 16);
-      acc[r][m] = v;
+      acc[r][m] = v * kTwo24;  // the partials are in units of 2^-24 (exact rescaling)
     }
   }
   if (t == 0 && kpart == 0) {
@@ -534,12 +544,15 @@ __global__ void __launch_bounds__(W * 32, 512 / (W * 32)) q4k_gemv_kernel(const 
   }
 }
 
-// Tuning knobs read once from the environment:
-//   JLLM_GEMV_CTAS_PER_SM  CTA target per SM for the configuration choice
-//   JLLM_GEMV_CFG          "R,W,KS" forces one configuration (when built)
-//   JLLM_GEMV_TRIGGER      where griddepcontrol.launch_dependents is issued:
-//                          0 never, 1 at entry, 2 after x staging, 3 at the end
-//   JLLM_GEMV_PRE          % of a CTA's warps whose rows are fetched before the wait
+// Launch-shape constants of the GEMV:
+//   ctas_per_sm  CTA target per SM for the configuration choice
+//   R, W, KS     one forced configuration (0: chosen per launch)
+//   trigger      where griddepcontrol.launch_dependents is issued:
+//                0 never, 1 at entry, 2 after x staging, 3 at the end
+//   pre_pct      % of a CTA's warps whose rows are fetched before the wait
+// They are fixed in the shipped library.  A build with -DJLLM_TUNING reads
+// overrides once from the environment (JLLM_GEMV_CTAS_PER_SM, JLLM_GEMV_CFG
+// = "R,W,KS", JLLM_GEMV_TRIGGER, JLLM_GEMV_PRE), for measurements only.
 struct Knobs {
   int ctas_per_sm = 2;
   int R = 0, W = 0, KS = 0;
@@ -549,10 +562,12 @@ struct Knobs {
 const Knobs& knobs() {
   static Knobs k = [] {
     Knobs v;
+#ifdef JLLM_TUNING
     if (const char* e = getenv("JLLM_GEMV_CTAS_PER_SM")) v.ctas_per_sm = atoi(e) < 1 ? 1 : atoi(e);
     if (const char* e = getenv("JLLM_GEMV_CFG")) sscanf(e, "%d,%d,%d", &v.R, &v.W, &v.KS);
     if (const char* e = getenv("JLLM_GEMV_TRIGGER")) v.trigger = atoi(e);
     if (const char* e = getenv("JLLM_GEMV_PRE")) v.pre_pct = atoi(e);
+#endif
     return v;
   }();
   return k;

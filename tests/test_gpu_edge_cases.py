@@ -1,0 +1,186 @@
+"""Matmul parity on the method's edge cases, for every matmul entry point.
+
+Weight rows mix random Q4_K blocks with closed-form ones (all-zero weights under
+a large scale, q = 15 with sc = 63, d = dmin = 0, any finite fp16 d/dmin,
+half-zero rows, pure-offset rows, subnormal d/dmin: tests/edge_inputs.py), and
+x mixes N(0,1) with values near 1e-4, fp16 subnormals and zeros.  Every output
+element is compared with the fp64 oracle at the bound
+|y - y_ref| <= 2e-3 * sum_k |x_k w_nk| + 1e-5; rows whose weights are all zero
+must come out exactly 0.
+"""
+import os
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+
+import oracle
+from edge_inputs import CAP_FINITE, CAP_FP16_OPERAND, N_KINDS, edge_weights, mixed_activations
+from gpu_helpers import assert_within, dev
+
+ZERO_KINDS = (1, 3)
+
+
+# ---------------------------------------------------------------- CPU checks of the inputs --
+
+def test_edge_rows_decode_as_described():
+    N, K = 2 * N_KINDS, 512
+    w = edge_weights(N, K, 11)
+    Wf = oracle.dequant(w, N, K, "f32").astype(np.float64)
+    for n in range(N):
+        kind = n % N_KINDS
+        if kind in ZERO_KINDS:
+            assert np.all(Wf[n] == 0.0), kind
+        if kind == 5:
+            sub = Wf[n].reshape(-1, 32)
+            assert np.all(sub[0::2] == 0.0) and np.any(sub[1::2] != 0.0)
+        if kind == 6:
+            assert np.all(Wf[n] <= 0.0)
+    x = mixed_activations(3, K, 12)
+    assert np.any((x != 0) & (np.abs(x.astype(np.float64)) < 2.0**-14))  # subnormals present
+    assert np.any(np.abs(x.astype(np.float64)) > 1.0)
+
+
+# ---------------------------------------------------------------------------- GPU parity --
+
+@pytest.fixture(scope="module")
+def q():
+    import bit_q4_weight_gb300
+
+    return bit_q4_weight_gb300
+
+
+def _zero_rows(w_kinds_N):
+    return np.array([n for n in range(w_kinds_N) if n % N_KINDS in ZERO_KINDS])
+
+
+def _check(y, w, x, N, K, label):
+    ref, s = oracle.matmul(w, x, N, K)
+    y = np.asarray(y, dtype=np.float64).reshape(ref.shape)
+    assert_within(y, ref, s, label)
+    z = _zero_rows(N)
+    assert np.all(y[:, z] == 0.0), f"{label}: all-zero weight rows must give exact zeros"
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("cap", [CAP_FP16_OPERAND, CAP_FINITE])
+@pytest.mark.parametrize("N,K", [(512, 2560), (129, 9728), (64, 4096)])
+def test_gemv_edge(q, N, K, cap):
+    w = edge_weights(N, K, 7000 + N + cap, cap_bits=cap)
+    x = mixed_activations(1, K, 7100 + N)
+    y = q.jllm_q4k_gemv(dev(w), dev(x.reshape(K)), N, K).cpu().numpy()
+    _check(y, w, x, N, K, f"gemv N={N} K={K} cap={cap:#x}")
+
+
+@pytest.mark.gpu
+def test_gemv_batch_edge(q):
+    K = 2560
+    Ns = [4096, 1024, 1024]
+    ws = [edge_weights(n, K, 7200 + i, cap_bits=CAP_FINITE) for i, n in enumerate(Ns)]
+    x = mixed_activations(1, K, 7300)
+    ys = q.jllm_q4k_gemv_batch([dev(w) for w in ws], dev(x.reshape(K)), Ns, K)
+    for i, (w, n, y) in enumerate(zip(ws, Ns, ys)):
+        _check(y.cpu().numpy(), w, x, n, K, f"gemv batch matrix {i}")
+
+
+@pytest.mark.gpu
+def test_gemv_rmsnorm_batch_edge(q):
+    K = 2560
+    Ns = [9728, 9728]
+    ws = [edge_weights(n, K, 7400 + i) for i, n in enumerate(Ns)]
+    x = mixed_activations(1, K, 7500)
+    gamma = np.random.Generator(np.random.PCG64(7501)).uniform(0.25, 2.0, size=K).astype(np.float32)
+    ys = q.jllm_q4k_gemv_rmsnorm_batch([dev(w) for w in ws], dev(x.reshape(K)), dev(gamma), 1e-6, Ns, K)
+    xn = oracle.rmsnorm(x.astype(np.float64), gamma.astype(np.float64), 1e-6)
+    for i, (w, n, y) in enumerate(zip(ws, Ns, ys)):
+        _check(y.cpu().numpy(), w, xn, n, K, f"rmsnorm gemv matrix {i}")
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("M", [2, 3, 4])
+def test_multi_token_gemv_edge(q, M):
+    import torch
+
+    N, K = 384, 2560
+    assert M <= q.jllm_q4k_gemv_max_m()
+    w = edge_weights(N, K, 7600 + M, cap_bits=CAP_FINITE)
+    x = mixed_activations(M, K, 7700 + M)
+    y = q.jllm_q4k_gemm(dev(w), dev(x), N, K, out_dtype=torch.float32).cpu().numpy()
+    _check(y, w, x, N, K, f"multi-token gemv M={M}")
+
+
+@pytest.mark.gpu
+def test_eight_token_gemv_edge_through_threshold_override():
+    """M = 5..8 through the 8-token GEMV kernel (threshold raised in a child process)."""
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    code = r'''
+import sys, numpy as np, torch
+sys.path.insert(0, sys.argv[1]); sys.path.insert(0, sys.argv[1] + "/tests")
+import bit_q4_weight_gb300 as q, oracle
+from edge_inputs import edge_weights, mixed_activations, CAP_FINITE
+assert q.jllm_q4k_gemv_max_m() == 8
+for M, N, K in ((5, 256, 2560), (8, 200, 9728)):
+    w = edge_weights(N, K, 7800 + M, cap_bits=CAP_FINITE); x = mixed_activations(M, K, 7900 + M)
+    ref, s = oracle.matmul(w, x, N, K)
+    y = q.jllm_q4k_gemm(torch.from_numpy(w).cuda(), torch.from_numpy(x).cuda(), N, K).cpu().numpy()
+    assert np.all(np.abs(y - ref) <= oracle.tolerance(s)), (M, N, K)
+    z = [n for n in range(N) if n % 8 in (1, 3)]
+    assert np.all(y[:, z] == 0.0)
+assert q.jllm_get_device_error() == 0
+print("ok")
+'''
+    env = dict(os.environ, JLLM_GEMV_MAX_M="8")
+    out = subprocess.run([sys.executable, "-c", code, root], env=env, capture_output=True, text=True, timeout=600)
+    assert out.returncode == 0 and out.stdout.strip().endswith("ok"), out.stderr[-2000:]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("M,split", [(33, True), (33, False), (2048, True), (235, True)])
+def test_tcgen05_gemm_edge(q, M, split):
+    """The tensor-core path (fp16 dequantised operands: d, dmin kept below 64)."""
+    import torch
+
+    N, K = 640 if M < 2048 else 384, 2560
+    w = edge_weights(N, K, 8000 + M)
+    x = mixed_activations(M, K, 8100 + M)
+    y = q.jllm_q4k_gemm(dev(w), dev(x), N, K, out_dtype=torch.float32, ws=None if split else False)
+    _check(y.cpu().numpy(), w, x, N, K, f"tcgen05 gemm M={M} split={split}")
+    assert q.jllm_get_device_error() == 0
+
+
+@pytest.mark.gpu
+def test_tcgen05_gemm_batch_edge(q):
+    import torch
+
+    K, M = 2560, 64
+    Ns = [512, 128, 136]
+    ws = [edge_weights(n, K, 8200 + i) for i, n in enumerate(Ns)]
+    x = mixed_activations(M, K, 8300)
+    ys = q.jllm_q4k_gemm_batch([dev(w) for w in ws], dev(x), Ns, K, out_dtype=torch.float32)
+    for i, (w, n, y) in enumerate(zip(ws, Ns, ys)):
+        _check(y.cpu().numpy(), w, x, n, K, f"gemm batch matrix {i}")
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("M", [1, 33])
+def test_swiglu_edge(q, M):
+    N, K = 320, 2560
+    # d, dmin below 2^-8 (the workloads' range) so that h = silu(g) * u stays within fp16
+    wg = edge_weights(N, K, 8400 + M, cap_bits=0x1C00)
+    wu = edge_weights(N, K, 8500 + M, cap_bits=0x1C00)
+    x = mixed_activations(M, K, 8600 + M)
+    h = q.jllm_q4k_ffn_swiglu(dev(wg), dev(wu), dev(x), N, K).float().cpu().numpy().astype(np.float64)
+    g, sg = oracle.matmul(wg, x, N, K)
+    u, su = oracle.matmul(wu, x, N, K)
+    href = oracle.swiglu(g, u)
+    tol = oracle.swiglu_tolerance(g, u, sg, su)
+    # fp16 output: where even the smallest value within the bound rounds beyond the fp16
+    # range (|h| >= 65520 rounds to inf), the result is inf of the reference's sign.
+    over = np.abs(href) - tol >= 65520.0
+    assert np.all(np.isinf(h[over]) & (np.sign(h[over]) == np.sign(href[over])))
+    fin = ~over & (np.abs(href) + tol < 65520.0)
+    err = np.abs(h[fin] - href[fin])
+    assert np.all(err <= tol[fin]), f"max excess {(err - tol[fin]).max()}"
+    z = _zero_rows(N)
+    assert np.all(h[:, z] == 0.0)

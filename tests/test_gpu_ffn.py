@@ -5,7 +5,7 @@ import pytest
 
 import oracle
 import synthetic
-from gpu_helpers import assert_within, dev, sample_cols
+from gpu_helpers import assert_within, dev, oracle_matmul_rows, sample_cols
 
 pytestmark = pytest.mark.gpu
 
@@ -64,18 +64,26 @@ def test_ffn_block(q, weights, M):
     rng = np.random.Generator(np.random.PCG64(M))
     cols = None if M == 1 else sample_cols(F, rng)
     href = _check_h(hn, weights["gate"], weights["up"], x, F, H, cols)
-    # down projection on the oracle's own fp16 h (computed from the oracle alone)
+    # down projection on the oracle's own fp16 h (computed from the oracle alone), every
+    # token row; at M = 512 the oracle's h comes from row chunks on several host threads
+    # and the down output is checked on sampled columns including the tail.
     if cols is None:
         h16 = href.astype(np.float16)
     else:
-        g, _ = oracle.matmul(weights["gate"], x[: min(M, 8)], F, H)
-        u, _ = oracle.matmul(weights["up"], x[: min(M, 8)], F, H)
+        g, _ = oracle_matmul_rows(weights["gate"], x, F, H)
+        u, _ = oracle_matmul_rows(weights["up"], x, F, H)
         h16 = oracle.swiglu(g, u).astype(np.float16)
+    assert h16.shape[0] == M
     # fp32 output: with these unnormalised synthetic magnitudes |y| reaches ~2.5e5,
     # beyond the fp16 range.
     y = q.jllm_q4k_gemm(dev(weights["down"]), dev(h16), H, F, out_dtype=torch.float32).cpu().numpy()
-    ref, s = oracle.matmul(weights["down"], h16, H, F)
-    assert_within(y, ref, s, f"down M={h16.shape[0]}")
+    if cols is None:
+        ref, s = oracle.matmul(weights["down"], h16, H, F)
+        assert_within(y, ref, s, f"down M={M}")
+    else:
+        dcols = sample_cols(H, rng, n_random=96)
+        ref, s = oracle_matmul_rows(weights["down"], h16, H, F, cols=dcols)
+        assert_within(y[:, dcols], ref, s, f"down M={M} (all rows, {len(dcols)} columns)")
 
 
 @pytest.mark.parametrize("M", [1, 512])
