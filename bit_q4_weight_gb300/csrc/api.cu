@@ -267,6 +267,9 @@ jllm_status jllm_get_device_error(jllm_stream_t stream) {
   uint32_t a = 0, b = 0;
   cudaError_t e = jllm::read_clear_gemm_error(&a, (cudaStream_t)stream);
   if (e == cudaSuccess) e = jllm::read_clear_gemv_error(&b);
+  // A tcgen05 kernel that gave up may have left stream-K flags set in the
+  // library's static workspace: clear them before anyone calls again.
+  if (e == cudaSuccess && a) e = jllm::gemm_static_workspace_reset((cudaStream_t)stream);
   if (e != cudaSuccess) return JLLM_ERR_CUDA;
   return (a | b) ? JLLM_ERR_DEVICE_TIMEOUT : JLLM_OK;
 }

@@ -46,6 +46,7 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -614,9 +615,13 @@ cudaError_t make_w_map(const void* w, int64_t N, int64_t K, CUtensorMap* mw) {
   return cudaSuccess;
 }
 
-// Tuning knobs read once from the environment:
-//   JLLM_GEMM_BN     tokens per tile (multiple of 16, at most the kernel's cap)
-//   JLLM_GEMM_SPLIT  0 keeps whole tiles even when a workspace is given
+// Launch-shape constants of the GEMM:
+//   bn     tokens per tile (0: chosen per launch; else a multiple of 16 up to
+//          the kernel's cap)
+//   split  0 keeps whole tiles even when a workspace is given
+// They are fixed in the shipped library.  A build with -DJLLM_TUNING reads
+// overrides once from the environment (JLLM_GEMM_BN, JLLM_GEMM_SPLIT), for
+// measurements only.
 struct GemmKnobs {
   int bn = 0;
   int split = 1;
@@ -624,8 +629,10 @@ struct GemmKnobs {
 const GemmKnobs& gemm_knobs() {
   static GemmKnobs k = [] {
     GemmKnobs v;
+#ifdef JLLM_TUNING
     if (const char* e = getenv("JLLM_GEMM_BN")) v.bn = atoi(e);
     if (const char* e = getenv("JLLM_GEMM_SPLIT")) v.split = atoi(e);
+#endif
     return v;
   }();
   return k;
@@ -671,6 +678,7 @@ constexpr int kMaxDevices = 64;
 void* g_static_ws_ptr[kMaxDevices];
 cudaError_t g_static_ws_err[kMaxDevices];
 std::once_flag g_static_ws_once[kMaxDevices];
+std::atomic<bool> g_static_ws_ready[kMaxDevices];
 
 }  // namespace
 
@@ -681,11 +689,30 @@ cudaError_t gemm_static_workspace(void** ptr, size_t* bytes) {
   if (d < 0 || d >= kMaxDevices) return cudaErrorInvalidDevice;
   std::call_once(g_static_ws_once[d], [d]() {
     g_static_ws_err[d] = cudaGetSymbolAddress(&g_static_ws_ptr[d], g_static_ws);
+    if (g_static_ws_err[d] == cudaSuccess) g_static_ws_ready[d].store(true);
   });
   if (g_static_ws_err[d] != cudaSuccess) return g_static_ws_err[d];
   *ptr = g_static_ws_ptr[d];
   *bytes = kStaticWsBytes;
   return cudaSuccess;
+}
+
+// After a kernel-side timeout the stream-K flag words of the static workspace
+// can be left non-zero (a contributor counted in, its finishing CTA gave up);
+// a later call would take them for fresh partial sums.  Return them to zero
+// (the partial slots need no clearing: a contributor rewrites its slot before
+// it counts in).  Nothing to do on a device whose array was never used.
+cudaError_t gemm_static_workspace_reset(cudaStream_t s) {
+  int d = 0;
+  cudaError_t e = cudaGetDevice(&d);
+  if (e != cudaSuccess) return e;
+  if (d < 0 || d >= kMaxDevices || !g_static_ws_ready[d].load()) return cudaSuccess;
+  const DevInfo& dev = device_info();
+  if (dev.err != cudaSuccess) return dev.err;
+  const size_t off = (size_t)dev.sm_count * SLOT_FLOATS * sizeof(float);
+  e = cudaMemsetAsync(static_cast<uint8_t*>(g_static_ws_ptr[d]) + off, 0, (size_t)dev.sm_count * sizeof(uint32_t), s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  return e;
 }
 
 size_t gemm_workspace_bytes() {

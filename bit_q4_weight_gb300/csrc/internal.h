@@ -61,6 +61,10 @@ size_t gemm_workspace_bytes();
 // looked up once per device, and its size).
 cudaError_t gemm_static_workspace(void** ptr, size_t* bytes);
 
+// Zero the stream-K flag words of the static workspace on the current device
+// (enqueued on s, then s is synchronised); a no-op if it was never used.
+cudaError_t gemm_static_workspace_reset(cudaStream_t s);
+
 // Read and clear the device error word of the tcgen05 kernels (after
 // synchronising the stream) and of the GEMV kernels.
 cudaError_t read_clear_gemm_error(uint32_t* bits, cudaStream_t s);

@@ -44,8 +44,11 @@
  * enqueued on `stream` and the call returns JLLM_OK without synchronising.
  * A launch failure returns JLLM_ERR_CUDA.  Kernel-side waits are bounded: a
  * wait that runs out sets a device error word that jllm_get_device_error()
- * reads.  No call throws, prints or keeps state beyond cached device
- * properties and a per-device table of driver entry points.
+ * reads.  No call throws or prints.  State kept: cached device properties,
+ * the driver's tensor-map encoder, and the static workspace of
+ * jllm_q4k_gemm_noalloc.  Environment variables read (once per process):
+ * JLLM_PDL and JLLM_GEMV_MAX_M, described below; no other setting changes
+ * launch shapes or summation order.
  * The GEMV and GEMM kernels are launched with programmatic dependent launch:
  * they start fetching W while the kernel enqueued just before them on the
  * same stream is still running, and read X / write Y (and the workspace)
@@ -178,6 +181,12 @@ jllm_status jllm_q4k_gemm(const void* w_q4k, const void* x, void* y, jllm_dtype 
  * Arguments and results as jllm_q4k_gemm without ws/ws_bytes.  The array
  * is shared by every call on a device, so calls must not overlap: issue
  * them on one stream (or order them), as with one caller workspace.
+ * The array belongs to the tcgen05 GEMM's module, so it is resident on
+ * every device that runs any tcgen05 GEMM of this library, whether or not
+ * this entry point is called.  Recovery: every call that completes leaves
+ * the array reusable; after a kernel-side timeout, jllm_get_device_error()
+ * (which reports it) also returns the array's flag words to zero, so call
+ * it before the next call on that device.
  * Errors: as jllm_q4k_gemm; WORKSPACE if the device has more SMs than the
  * array was sized for.
  */
@@ -248,8 +257,11 @@ size_t jllm_q4k_workspace_bytes(int64_t M, int64_t N, int64_t K);
 int jllm_q4k_gemv_max_m(void);
 
 /*
- * Synchronise `stream`, then read and clear the device error word that a
- * kernel sets when one of its bounded waits runs out.  Returns JLLM_OK,
+ * Synchronise `stream`, then read and clear the device error words (current
+ * device) that a kernel sets when one of its bounded waits runs out.  When a
+ * tcgen05 GEMM timed out, the stream-K flags of the library's static
+ * workspace (jllm_q4k_gemm_noalloc) are zeroed as well; a caller-owned
+ * workspace must be zero-filled again by its owner.  Returns JLLM_OK,
  * JLLM_ERR_DEVICE_TIMEOUT or JLLM_ERR_CUDA.
  */
 jllm_status jllm_get_device_error(jllm_stream_t stream);

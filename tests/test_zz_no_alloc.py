@@ -31,11 +31,13 @@ def test_noalloc_matches_oracle_and_caller_workspace(q, N, K, M):
     y2 = torch.empty_like(y)
     q.jllm_q4k_gemm_noalloc(wd, xd, N, K, out=y)  # first use loads the module (and its static array)
     torch.cuda.synchronize()
-    before = torch.cuda.mem_get_info()[0]
+    # Process-local counters (torch's allocator) and the device-wide free memory; the
+    # latter assumes no other process allocates on this GPU meanwhile.
+    before = (torch.cuda.memory_allocated(), torch.cuda.memory_reserved(), torch.cuda.mem_get_info()[0])
     q.jllm_q4k_gemm_noalloc(wd, xd, N, K, out=y)
     q.jllm_q4k_gemm_noalloc(wd, xd, N, K, out=y2)
     torch.cuda.synchronize()
-    after = torch.cuda.mem_get_info()[0]
+    after = (torch.cuda.memory_allocated(), torch.cuda.memory_reserved(), torch.cuda.mem_get_info()[0])
     assert after == before  # the calls allocate no device memory
     assert_within(y.cpu().numpy(), ref, s, f"noalloc N={N} K={K} M={M}")
     assert torch.equal(y, y2)  # the static workspace is left reusable
