@@ -19,6 +19,10 @@ Every function restates a definition in plain single-threaded C, fp64:
 * ``rmsnorm`` -- xn = x * gamma / sqrt(mean(x^2) + eps) per token row (the
   RMSNorm of the same kernel bullet; the standard root-mean-square norm, named
   but not printed on the pages), the prologue of the fused-norm GEMV.
+* ``rope`` -- rotary position embedding of head vectors (pairs (i, i + D/2),
+  angle pos * base^(-2i/D)), the RoPE of the same kernel bullet; the pages
+  print no formula, this is the form of the Qwen3 model they run.
+  ``head_rmsnorm`` -- ``rmsnorm`` applied per head vector (Qwen3's q/k norm).
 * ``quantize`` -- a plain non-iterative quantiser used only for the round-trip
   pin (not on the pages; the rule is stated in q4k_oracle.c).
 
@@ -79,6 +83,8 @@ def _load():
     lib.oq_swiglu.restype = None
     lib.oq_rmsnorm.argtypes = [P, P, I64, I64, ctypes.c_double, P]
     lib.oq_rmsnorm.restype = None
+    lib.oq_rope.argtypes = [P, I64, I64, I64, ctypes.c_double, P]
+    lib.oq_rope.restype = None
     lib.oq_quantize_block.argtypes = [P, P]
     lib.oq_quantize_block.restype = None
     lib.oq_quantize.argtypes = [P, I64, I64, P]
@@ -208,6 +214,26 @@ def rmsnorm(x: np.ndarray, gamma: np.ndarray, eps: float) -> np.ndarray:
     out = np.empty_like(xa)
     _load().oq_rmsnorm(_ptr(xa), _ptr(gamma), xa.shape[0], K, float(eps), _ptr(out))
     return out.reshape(np.asarray(x).shape)
+
+
+def rope(v: np.ndarray, pos: int, base: float, head_dim: int = 128) -> np.ndarray:
+    """Rotary position embedding of head vectors ([..., head_dim] fp64; pairs (i, i + head_dim/2),
+    angle pos * base^(-2i/head_dim)), fp64."""
+    if head_dim % 2:
+        raise ValueError("head_dim must be even")
+    va = np.ascontiguousarray(np.asarray(v, dtype=np.float64))
+    if va.size % head_dim:
+        raise ValueError("size must be a multiple of head_dim")
+    out = np.empty_like(va)
+    _load().oq_rope(_ptr(va), va.size // head_dim, head_dim, int(pos), float(base), _ptr(out))
+    return out
+
+
+def head_rmsnorm(v: np.ndarray, gamma: np.ndarray, eps: float, head_dim: int = 128) -> np.ndarray:
+    """RMSNorm of every head vector of v (the per-head q/k norm that Qwen3 applies before
+    RoPE): ``rmsnorm`` on v viewed as [heads, head_dim] rows, gamma [head_dim]."""
+    va = np.asarray(v, dtype=np.float64)
+    return rmsnorm(va.reshape(-1, head_dim), gamma, eps).reshape(va.shape)
 
 
 def quantize(w: np.ndarray) -> np.ndarray:

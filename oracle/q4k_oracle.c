@@ -245,6 +245,33 @@ void oq_rmsnorm(const double* x, const double* gamma, int64_t M, int64_t K, doub
   }
 }
 
+/* ----------------------------------------------------------------- RoPE --- */
+
+/* Rotary position embedding of n_heads head vectors of head_dim values each
+ * (head_dim even, half = head_dim/2), at position pos, fp64: the "RoPE" of the
+ * README's "fused RMSNorm + RoPE + SwiGLU" kernel.  The pages print neither
+ * the pairing nor the frequencies; this is the form used by Qwen3 (the model
+ * the pages run): value i of a head is paired with value i + half, the pair
+ * is rotated by the angle pos * theta_i with theta_i = base^(-2i/head_dim):
+ *   out[i]        = v[i] * cos(a) - v[i + half] * sin(a)
+ *   out[i + half] = v[i + half] * cos(a) + v[i] * sin(a)
+ * in_place allowed (out == v). */
+void oq_rope(const double* v, int64_t n_heads, int64_t head_dim, int64_t pos, double base, double* out) {
+  const int64_t half = head_dim / 2;
+  for (int64_t h = 0; h < n_heads; h++) {
+    const double* vh = v + h * head_dim;
+    double* oh = out + h * head_dim;
+    for (int64_t i = 0; i < half; i++) {
+      const double theta = pow(base, -2.0 * (double)i / (double)head_dim);
+      const double a = (double)pos * theta;
+      const double c = cos(a), sn = sin(a);
+      const double x0 = vh[i], x1 = vh[i + half];
+      oh[i] = x0 * c - x1 * sn;
+      oh[i + half] = x1 * c + x0 * sn;
+    }
+  }
+}
+
 /* ------------------------------------------------------------ quantiser --- */
 
 /* Smallest binary16 value >= v (v >= 0, finite, below 65504), as bits. */

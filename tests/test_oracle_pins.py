@@ -373,6 +373,76 @@ def test_rmsnorm_invariants():
         assert np.array_equal(oracle.rmsnorm(x[m:m + 1], g, 1e-6)[0], oracle.rmsnorm(x[m], g, 1e-6))
 
 
+# ------------------------------------------------------------------- RoPE ----
+
+QWEN3_ROPE_BASE = 1.0e6
+
+
+def test_rope_identity_at_position_zero():
+    rng = np.random.Generator(np.random.PCG64(80))
+    v = rng.standard_normal((3, 128))
+    assert np.array_equal(oracle.rope(v, 0, QWEN3_ROPE_BASE), v)  # cos 0 = 1, sin 0 = 0 exactly
+
+
+def test_rope_unit_vectors_pin_pairing_sign_and_frequencies():
+    # Pair i rotates (e_i, e_{i+64}) counter-clockwise by pos * base^(-i/64): e_i goes to
+    # cos a * e_i + sin a * e_{i+64}, e_{i+64} to -sin a * e_i + cos a * e_{i+64}.
+    # Frequency 0 is exactly 1 rad per position: cos 1 = 0.5403023058681398, sin 1 = 0.8414709848078965.
+    e0 = np.zeros(128)
+    e0[0] = 1.0
+    r = oracle.rope(e0, 1, QWEN3_ROPE_BASE)
+    assert r[0] == pytest.approx(0.5403023058681398, abs=1e-16)
+    assert r[64] == pytest.approx(0.8414709848078965, abs=1e-16)
+    assert np.count_nonzero(r) == 2
+    for i, pos in ((1, 7), (32, 1000), (63, 32767)):
+        a = pos * QWEN3_ROPE_BASE ** (-i / 64.0)
+        for src, want in ((i, {i: math.cos(a), i + 64: math.sin(a)}), (i + 64, {i: -math.sin(a), i + 64: math.cos(a)})):
+            v = np.zeros(128)
+            v[src] = 1.0
+            r = oracle.rope(v, pos, QWEN3_ROPE_BASE)
+            for k, val in want.items():
+                assert r[k] == pytest.approx(val, abs=1e-12), (i, pos, src, k)
+            assert np.count_nonzero(r) <= 2
+    # the lowest frequency with base 10^6 and head size 128: 10^(-6*63/64) rad per position
+    v = np.zeros(128)
+    v[63] = 1.0
+    a = 1e5 * 10.0 ** (-6.0 * 63.0 / 64.0)
+    assert oracle.rope(v, 100000, QWEN3_ROPE_BASE)[127] == pytest.approx(math.sin(a), abs=1e-12)
+
+
+def test_rope_preserves_pair_norms_and_composes():
+    rng = np.random.Generator(np.random.PCG64(81))
+    v = rng.standard_normal((4, 128)) * 3.0
+    r = oracle.rope(v, 12345, QWEN3_ROPE_BASE)
+    n0 = v[:, :64] ** 2 + v[:, 64:] ** 2
+    n1 = r[:, :64] ** 2 + r[:, 64:] ** 2
+    assert np.allclose(n1, n0, rtol=1e-13, atol=1e-13)
+    # rotation by p1 then p2 equals rotation by p1 + p2; by p then -p is the identity
+    for p1, p2 in ((3, 5), (1000, 24), (20000, 12767)):
+        a = oracle.rope(oracle.rope(v, p1, QWEN3_ROPE_BASE), p2, QWEN3_ROPE_BASE)
+        b = oracle.rope(v, p1 + p2, QWEN3_ROPE_BASE)
+        assert np.allclose(a, b, rtol=0, atol=1e-9)
+    back = oracle.rope(oracle.rope(v, 777, QWEN3_ROPE_BASE), -777, QWEN3_ROPE_BASE)
+    assert np.allclose(back, v, rtol=0, atol=1e-12)
+    # heads are independent and linear: the rotation of a sum is the sum of rotations
+    w = rng.standard_normal((4, 128))
+    lhs = oracle.rope(v + 2.0 * w, 99, QWEN3_ROPE_BASE)
+    rhs = oracle.rope(v, 99, QWEN3_ROPE_BASE) + 2.0 * oracle.rope(w, 99, QWEN3_ROPE_BASE)
+    assert np.allclose(lhs, rhs, rtol=0, atol=1e-12)
+
+
+def test_head_rmsnorm_is_rmsnorm_per_head():
+    rng = np.random.Generator(np.random.PCG64(82))
+    v = rng.standard_normal(8 * 128) * np.repeat(rng.uniform(0.1, 10.0, size=8), 128)
+    g = rng.uniform(0.5, 1.5, size=128)
+    hn = oracle.head_rmsnorm(v, g, 1e-6).reshape(8, 128)
+    for h in range(8):
+        seg = v[h * 128:(h + 1) * 128]
+        assert np.array_equal(hn[h], oracle.rmsnorm(seg, g, 1e-6))
+        # unit root-mean-square per head before gamma (eps negligible here)
+        assert np.mean((hn[h] / g) ** 2) == pytest.approx(1.0, rel=1e-5)
+
+
 def test_synthetic_weights_distribution():
     w = synthetic.q4k_weights(64, 2560, seed=1)
     assert w.shape == (64, 10 * 144)
