@@ -41,6 +41,7 @@ EXPORTS = (
     "jllm_q4k_gemv",
     "jllm_q4k_gemv_batch",
     "jllm_q4k_gemv_rmsnorm_batch",
+    "jllm_q4k_gemv_qkv_rope",
     "jllm_q4k_gemm",
     "jllm_q4k_gemm_noalloc",
     "jllm_q4k_gemm_batch",
@@ -78,6 +79,9 @@ lib.jllm_q4k_gemv_batch.argtypes = [_P, _P, _P, ctypes.c_int, _P, _I64, _P]
 lib.jllm_q4k_gemv_batch.restype = _ST
 lib.jllm_q4k_gemv_rmsnorm_batch.argtypes = [_P, _P, _P, ctypes.c_int, _P, _P, ctypes.c_float, _I64, _P]
 lib.jllm_q4k_gemv_rmsnorm_batch.restype = _ST
+lib.jllm_q4k_gemv_qkv_rope.argtypes = [_P, _P, _I64, _I64, _P, _I64, _P, ctypes.c_float, _P, _P, ctypes.c_float,
+                                       _I64, ctypes.c_float, _P]
+lib.jllm_q4k_gemv_qkv_rope.restype = _ST
 lib.jllm_q4k_gemm.argtypes = [_P, _P, _P, ctypes.c_int, _I64, _I64, _I64, _P, _SZ, _P]
 lib.jllm_q4k_gemm.restype = _ST
 lib.jllm_q4k_gemm_noalloc.argtypes = [_P, _P, _P, ctypes.c_int, _I64, _I64, _I64, _P]
@@ -261,6 +265,38 @@ def jllm_q4k_gemv_rmsnorm_batch(ws_q4k, x, gamma, eps: float, Ns, K: int, outs=N
     npa = (ctypes.c_int64 * cnt)(*Ns)
     _check(lib.jllm_q4k_gemv_rmsnorm_batch(wp, yp, npa, cnt, x.data_ptr(), gamma.data_ptr(), float(eps), K,
                                            _stream_ptr(stream)), "jllm_q4k_gemv_rmsnorm_batch")
+    return outs
+
+
+def jllm_q4k_gemv_qkv_rope(w_qkv, x, n_q_heads: int, n_kv_heads: int, K: int, pos: int, rope_base: float = 1e6,
+                           gamma=None, eps: float = 1e-6, q_gamma=None, k_gamma=None, head_eps: float = 1e-6,
+                           outs=None, stream=None):
+    """(q, k, v) fp32 of one fp16 token x[K]: the three projections in one launch, RoPE at `pos`
+    on q and k (heads of 128), optional RMSNorm of x (gamma [K]) and per-head RMSNorm of q / k
+    (q_gamma, k_gamma [128])."""
+    torch = _torch()
+    w_qkv = list(w_qkv)
+    if len(w_qkv) != 3:
+        raise ValueError("three matrices: Wq, Wk, Wv")
+    Ns = [n_q_heads * 128, n_kv_heads * 128, n_kv_heads * 128]
+    for i, (w, n) in enumerate(zip(w_qkv, Ns)):
+        _need(w, torch.uint8, _w_shape(n, K), f"w[{i}]")
+    if x.dim() == 2 and x.shape[0] == 1:
+        x = x.view(K)
+    _need(x, torch.float16, (K,), "x")
+    for name, g, n in (("gamma", gamma, K), ("q_gamma", q_gamma, 128), ("k_gamma", k_gamma, 128)):
+        if g is not None:
+            _need(g, torch.float32, (n,), name)
+    if outs is None:
+        outs = [torch.empty((n,), dtype=torch.float32, device=x.device) for n in Ns]
+    for i, (o, n) in enumerate(zip(outs, Ns)):
+        _need(o, torch.float32, (n,), f"out[{i}]")
+    wp = (ctypes.c_void_p * 3)(*[w.data_ptr() for w in w_qkv])
+    yp = (ctypes.c_void_p * 3)(*[o.data_ptr() for o in outs])
+    ptr = lambda t: t.data_ptr() if t is not None else None
+    _check(lib.jllm_q4k_gemv_qkv_rope(wp, yp, n_q_heads, n_kv_heads, x.data_ptr(), K, ptr(gamma), float(eps),
+                                      ptr(q_gamma), ptr(k_gamma), float(head_eps), int(pos), float(rope_base),
+                                      _stream_ptr(stream)), "jllm_q4k_gemv_qkv_rope")
     return outs
 
 

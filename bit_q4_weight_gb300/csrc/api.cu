@@ -2,6 +2,7 @@
 // M-threshold dispatch between the GEMV and the tcgen05 GEMM, and status
 // mapping.  Nothing here allocates device memory.
 #include <cuda_runtime.h>
+#include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
 
@@ -185,6 +186,36 @@ jllm_status jllm_q4k_gemv_rmsnorm_batch(const void* const* w_q4k, float* const* 
                                                    eps, K, (cudaStream_t)stream));
 }
 
+jllm_status jllm_q4k_gemv_qkv_rope(const void* const* w_q4k, float* const* y, int64_t n_q_heads,
+                                   int64_t n_kv_heads, const void* x, int64_t K, const float* gamma, float eps,
+                                   const float* q_gamma, const float* k_gamma, float head_eps, int64_t pos,
+                                   float rope_base, jllm_stream_t stream) {
+  if (!w_q4k || !y || !x) return JLLM_ERR_INVALID_ARG;
+  if (n_q_heads < 1 || n_kv_heads < 1) return JLLM_ERR_INVALID_ARG;
+  if (gamma && (!(eps >= 0.f) || eps > 1.f)) return JLLM_ERR_INVALID_ARG;
+  if ((q_gamma || k_gamma) && (!(head_eps >= 0.f) || head_eps > 1.f)) return JLLM_ERR_INVALID_ARG;
+  if (!(rope_base > 0.f) || !isfinite(rope_base)) return JLLM_ERR_INVALID_ARG;
+  if (pos < INT32_MIN || pos > INT32_MAX) return JLLM_ERR_INVALID_ARG;
+  if (!aligned16(x) || (gamma && !aligned16(gamma)) || (q_gamma && !aligned16(q_gamma)) ||
+      (k_gamma && !aligned16(k_gamma)))
+    return JLLM_ERR_MISALIGNED;
+  const int64_t head = 128;
+  if (n_q_heads > kMaxRows / head || n_kv_heads > kMaxRows / head) return JLLM_ERR_UNSUPPORTED_SHAPE;
+  const int64_t N[3] = {n_q_heads * head, n_kv_heads * head, n_kv_heads * head};
+  for (int i = 0; i < 3; ++i) {
+    if (!w_q4k[i] || !y[i]) return JLLM_ERR_INVALID_ARG;
+    jllm_status st = check_shape(1, N[i], K);
+    if (st != JLLM_OK) return st;
+    if (!aligned16(w_q4k[i]) || !aligned16(y[i])) return JLLM_ERR_MISALIGNED;
+  }
+  if (N[0] + N[1] + N[2] > kMaxRows) return JLLM_ERR_UNSUPPORTED_SHAPE;
+  jllm_status st = check_device();
+  if (st != JLLM_OK) return st;
+  const float* hg[2] = {q_gamma, k_gamma};
+  return from_cuda(jllm::launch_gemv_qkv_rope(w_q4k, reinterpret_cast<void* const*>(y), N, 2, hg, head_eps, (int)pos,
+                                              (double)rope_base, x, gamma, eps, K, (cudaStream_t)stream));
+}
+
 jllm_status jllm_q4k_gemm(const void* w_q4k, const void* x, void* y, jllm_dtype y_dt, int64_t M, int64_t N,
                           int64_t K, void* ws, size_t ws_bytes, jllm_stream_t stream) {
   if (!w_q4k || !x || !y) return JLLM_ERR_INVALID_ARG;
@@ -273,5 +304,16 @@ jllm_status jllm_get_device_error(jllm_stream_t stream) {
   if (e != cudaSuccess) return JLLM_ERR_CUDA;
   return (a | b) ? JLLM_ERR_DEVICE_TIMEOUT : JLLM_OK;
 }
+
+#ifdef JLLM_FAULT_INJECTION
+// Test builds only (not declared in the public header): gemm_skip_x makes CTA
+// 0 of the next tcgen05 GEMMs skip its first X copy, gemv_skip_w makes warp 0
+// of CTA 0 of the next GEMVs skip its weight copy; 0 clears either.
+jllm_status jllm_test_fault_injection(int gemm_skip_x, int gemv_skip_w) {
+  cudaError_t e = jllm::fault_injection_set_gemm(gemm_skip_x);
+  if (e == cudaSuccess) e = jllm::fault_injection_set_gemv(gemv_skip_w);
+  return from_cuda(e);
+}
+#endif
 
 }  // extern "C"

@@ -57,6 +57,13 @@ namespace {
 
 __device__ uint32_t g_gemm_error;
 
+#ifdef JLLM_FAULT_INJECTION
+// Test builds only: when set, the producer of CTA 0 never issues its first X
+// copy, so the MMA warp's bounded wait on that stage runs out and the whole
+// timeout path runs (error word, abort flag, wind-down, TMEM freed).
+__device__ int g_fi_skip_x;
+#endif
+
 __device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t mask, uint32_t orv) {
   uint32_t r;
   asm("lop3.b32 %0, %1, %2, %3, 0xea;" : "=r"(r) : "r"(a), "r"(mask), "r"(orv));  // (a & b) | c
@@ -103,7 +110,10 @@ constexpr int NUM_EPI_WARPS = 4;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COLS = 256;                  // TMEM columns per accumulator buffer
 constexpr int SLOT_FLOATS = TILE_N * 256;           // fp32 partial of one tile (128 KiB)
-constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;   // 2 s
+#ifndef JLLM_WAIT_LIMIT_NS
+#define JLLM_WAIT_LIMIT_NS 2000000000ull
+#endif
+constexpr uint64_t WAIT_LIMIT_NS = JLLM_WAIT_LIMIT_NS;  // 2 s (a test build shortens it)
 
 template <bool SWIGLU>
 struct Cfg {
@@ -294,8 +304,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             break;
           }
           if (nx == 0) pdl_wait();  // X may come from the previous kernel; the weights do not
-          mbar_arrive_expect_tx(b_xfull + 8 * rx.s, p.x_stage_bytes);
-          tma_load_2d(sx + (uint32_t)rx.s * p.x_stage_bytes, &tmX, b_xfull + 8 * rx.s, k * KSTEP, m0);
+#ifdef JLLM_FAULT_INJECTION
+          if (!(nx == 0 && blockIdx.x == 0 && g_fi_skip_x))
+#endif
+          {
+            mbar_arrive_expect_tx(b_xfull + 8 * rx.s, p.x_stage_bytes);
+            tma_load_2d(sx + (uint32_t)rx.s * p.x_stage_bytes, &tmX, b_xfull + 8 * rx.s, k * KSTEP, m0);
+          }
           rx.next();
           ++nx;
         }
@@ -824,6 +839,10 @@ cudaError_t launch_gemm_tc_batch(const void* const* w, const int64_t* N, int cou
                                  bool y_f16, int64_t M, int64_t K, void* ws, size_t ws_bytes, cudaStream_t s) {
   return launch_tc_common(w, nullptr, N, count, x, y, y_f16, M, K, ws, ws_bytes, s);
 }
+
+#ifdef JLLM_FAULT_INJECTION
+cudaError_t fault_injection_set_gemm(int skip_x) { return cudaMemcpyToSymbol(g_fi_skip_x, &skip_x, sizeof(int)); }
+#endif
 
 cudaError_t read_clear_gemm_error(uint32_t* bits, cudaStream_t s) {
   cudaError_t e = cudaStreamSynchronize(s);

@@ -47,6 +47,7 @@
 // SWIGLU mode computes the gate/up pair of a SwiGLU MLP in the same pass:
 // a group's weight rows alternate gate row n / up row n, and the output is
 // h[n] = silu(g) * u in fp16.
+#include <math.h>
 #include <stdio.h>
 #include <stdlib.h>
 
@@ -201,7 +202,16 @@ constexpr float kTwoM24 = 5.9604644775390625e-8f;  // 2^-24
 constexpr float kTwo24 = 16777216.0f;              // 2^24
 
 __device__ uint32_t g_gemv_error;
-constexpr uint64_t GEMV_WAIT_LIMIT_NS = 2000000000ull;  // 2 s
+#ifndef JLLM_WAIT_LIMIT_NS
+#define JLLM_WAIT_LIMIT_NS 2000000000ull
+#endif
+constexpr uint64_t GEMV_WAIT_LIMIT_NS = JLLM_WAIT_LIMIT_NS;  // 2 s (a test build shortens it)
+
+#ifdef JLLM_FAULT_INJECTION
+// Test builds only: when set, warp 0 of CTA 0 never issues its weight copy, so
+// its bounded wait runs out and the GEMV's timeout path runs.
+__device__ int g_fi_skip_w;
+#endif
 
 // The matrices of one launch.  Matrix i owns CTAs [cta0[i], cta0[i+1]).
 struct GemvBatch {
@@ -210,14 +220,26 @@ struct GemvBatch {
   int n[kMaxGemvBatch];
   int cta0[kMaxGemvBatch];
   int count;
+  // Rotary epilogue (ROPE kernels): matrix i with bit i of rope_mask set holds
+  // heads of 128 rows; hgamma[i] is its per-head RMSNorm weight [128]
+  // (nullptr: no per-head norm).  Angle of pair j at position pos:
+  // pos * 2^(-(j/64) * log2_base).
+  const float* hgamma[kMaxGemvBatch];
+  unsigned rope_mask;
+  int rope_pos;
+  double rope_log2_base;
+  float head_eps;
 };
+
+constexpr int kHeadDim = 128;     // rows per head in the rotary epilogue
+constexpr int kRopeCluster = 8;   // CTAs per head (16 rows = 8 rotation pairs each)
 
 // One CTA: W warps x 4 groups x R weight rows, K walked in chunks of KC
 // blocks (one chunk whenever the rows fit, which covers the model shapes).
 // Per chunk, warp w's rows arrive by bulk copy on the warp's own mbarrier --
 // a single copy when the chunk is the whole row, since the warp's rows are
 // then contiguous in W -- and each warp starts as soon as its rows land.
-template <int R, int W, int KS, bool SWIGLU, int MT, bool NORM>
+template <int R, int W, int KS, bool SWIGLU, int MT, bool NORM, bool ROPE>
 __global__ void __launch_bounds__(W * 32, 512 / (W * 32)) q4k_gemv_kernel(const __grid_constant__ GemvBatch batch,
                                                           const uint8_t* __restrict__ W1,
                                                           const __half* __restrict__ x, int NB, int KC,
@@ -238,6 +260,8 @@ __global__ void __launch_bounds__(W * 32, 512 / (W * 32)) q4k_gemv_kernel(const 
   const uint8_t* W0 = batch.w[0];
   void* y = batch.y[0];
   int N = batch.n[0], cta0 = 0;
+  const float* hgamma = batch.hgamma[0];
+  bool rope = ROPE && (batch.rope_mask & 1u);
 #pragma unroll
   for (int i = 1; i < kMaxGemvBatch; ++i) {
     if (i < batch.count && (int)blockIdx.x >= batch.cta0[i]) {
@@ -245,8 +269,14 @@ __global__ void __launch_bounds__(W * 32, 512 / (W * 32)) q4k_gemv_kernel(const 
       y = batch.y[i];
       N = batch.n[i];
       cta0 = batch.cta0[i];
+      if (ROPE) {
+        hgamma = batch.hgamma[i];
+        rope = (batch.rope_mask >> i) & 1u;
+      }
     }
   }
+  static_assert(!ROPE || (R == 1 && W == 4 && KS == 1 && !SWIGLU && MT == 1),
+                "the rotary epilogue is laid out for 4 warps x 4 single-row groups");
 
   const int64_t row_bytes = (int64_t)NB * BLOCK_BYTES;   // global row pitch
   const int srow = KC * BLOCK_BYTES;                       // shared row pitch
@@ -261,7 +291,13 @@ __global__ void __launch_bounds__(W * 32, 512 / (W * 32)) q4k_gemv_kernel(const 
   const int rset = grp / KS, kpart = grp % KS;
   const LaneDec L = lane_dec(c);
   const int64_t n_cta = (int64_t)((int)blockIdx.x - cta0) * (W * RS * RP);
-  const int64_t n_warp = n_cta + (int64_t)warp * RS * RP;
+  // Rotary matrices: the 8 CTAs of a cluster share one head; CTA rank cr owns
+  // rows 8cr..8cr+7 (warps 0, 1) and their rotation partners 64+8cr..64+8cr+7
+  // (warps 2, 3), four contiguous rows per warp.
+  const int ccta = (int)blockIdx.x - cta0, crank = ccta & (kRopeCluster - 1);
+  const int64_t n_warp = rope ? (int64_t)(ccta / kRopeCluster) * kHeadDim + (warp >= 2 ? kHeadDim / 2 : 0) +
+                                    8 * crank + 4 * (warp & 1)
+                              : n_cta + (int64_t)warp * RS * RP;
   const int rows_w = (int)(N - n_warp < RS * RP ? (N - n_warp > 0 ? N - n_warp : 0) : RS * RP);
   const int nchunks = (NB + KC - 1) / KC;
 
@@ -282,6 +318,9 @@ __global__ void __launch_bounds__(W * 32, 512 / (W * 32)) q4k_gemv_kernel(const 
     const uint32_t dst = smem_u32(tile + (size_t)warp * ROWS_W * srow);
     const uint32_t total = (uint32_t)rows_w * row_chunk * (SWIGLU ? 2 : 1);
     const uint64_t pol = l2_policy_evict_first();  // weights are read once per call
+#ifdef JLLM_FAULT_INJECTION
+    if (ch == 0 && warp == 0 && blockIdx.x == 0 && g_fi_skip_w) return;
+#endif
     if (lane == 0) mbar_arrive_expect_tx(bar, total);
     __syncwarp();
     if (kc == NB) {
@@ -522,7 +561,46 @@ __global__ void __launch_bounds__(W * 32, 512 / (W * 32)) q4k_gemv_kernel(const 
       acc[r][m] = v * kTwo24;  // the partials are in units of 2^-24 (exact rescaling)
     }
   }
-  if (t == 0 && kpart == 0) {
+  if (ROPE && rope) {
+    // Rotary epilogue of one 16-row slice of a head: per-head RMSNorm (sum of
+    // squares reduced over the cluster through distributed shared memory, in
+    // rank order), then the rotation of pairs (j, j + 64), j = 8 cr + p.
+    __shared__ float rv[16];
+    __shared__ float hred[kRopeCluster];
+    if (t == 0) rv[4 * warp + grp] = acc[0][0];
+    __syncthreads();
+    float r = 1.f;
+    if (hgamma != nullptr) {
+      if (threadIdx.x == 0) {
+        float ss = 0.f;
+#pragma unroll
+        for (int l = 0; l < 16; ++l) ss = fmaf(rv[l], rv[l], ss);
+        const uint32_t slot = smem_u32(&hred[crank]);
+#pragma unroll
+        for (int dst = 0; dst < kRopeCluster; ++dst) st_cluster_f32(mapa_shared(slot, (uint32_t)dst), ss);
+      }
+      cluster_sync_all();
+      float tot = 0.f;
+#pragma unroll
+      for (int i = 0; i < kRopeCluster; ++i) tot += hred[i];
+      r = 1.f / sqrtf(tot / (float)kHeadDim + batch.head_eps);
+    }
+    if (threadIdx.x < 8) {
+      const int p = threadIdx.x, j = 8 * crank + p;
+      float a = rv[p], b = rv[p + 8];
+      if (hgamma != nullptr) {
+        a = __fmul_rn(__fmul_rn(a, r), hgamma[j]);
+        b = __fmul_rn(__fmul_rn(b, r), hgamma[j + kHeadDim / 2]);
+      }
+      // angle pos * base^(-2j/128) in fp64 (exact enough at any position), then fp32
+      double sd, cd;
+      sincos((double)batch.rope_pos * exp2(-(double)j / (kHeadDim / 2) * batch.rope_log2_base), &sd, &cd);
+      const float c = (float)cd, sn = (float)sd;
+      float* yo = reinterpret_cast<float*>(y) + (int64_t)(ccta / kRopeCluster) * kHeadDim;
+      yo[j] = __fsub_rn(__fmul_rn(a, c), __fmul_rn(b, sn));
+      yo[j + kHeadDim / 2] = __fadd_rn(__fmul_rn(b, c), __fmul_rn(a, sn));
+    }
+  } else if (t == 0 && kpart == 0) {
     const int64_t nb = n_warp + (int64_t)rset * RP;
 #pragma unroll
     for (int i = 0; i < RP; ++i) {
@@ -609,9 +687,15 @@ struct GemvJob {
   int out_f16;
   const float* gamma = nullptr;  // RMSNorm weight [K] (one token only), else nullptr
   float eps = 0.f;
+  // rotary epilogue (see GemvBatch)
+  unsigned rope_mask = 0;
+  const float* hgamma[kMaxGemvBatch] = {};
+  int rope_pos = 0;
+  double rope_log2_base = 0.0;
+  float head_eps = 0.f;
 };
 
-template <int R, int W, int KS, bool SWIGLU, int MT, bool NORM = false>
+template <int R, int W, int KS, bool SWIGLU, int MT, bool NORM = false, bool ROPE = false>
 cudaError_t launch_gemv_cfg(const GemvJob& job, cudaStream_t stream, bool pdl, int trigger, int pre_pct) {
   const int NB = (int)(job.K / QK);
   constexpr int RP = SWIGLU ? R / 2 : R;
@@ -628,10 +712,23 @@ cudaError_t launch_gemv_cfg(const GemvJob& job, cudaStream_t stream, bool pdl, i
     grid += (job.n[i] + rows_per_cta - 1) / rows_per_cta;
   }
   b.count = job.count;
+  if (ROPE) {
+    for (int i = 0; i < job.count; ++i) {
+      if (job.rope_mask >> i & 1u) {
+        if (job.n[i] % kHeadDim) return cudaErrorInvalidValue;
+        b.hgamma[i] = job.hgamma[i];
+      }
+      if (job.n[i] % (rows_per_cta * kRopeCluster)) return cudaErrorInvalidValue;  // whole clusters per matrix
+    }
+    b.rope_mask = job.rope_mask;
+    b.rope_pos = job.rope_pos;
+    b.rope_log2_base = job.rope_log2_base;
+    b.head_eps = job.head_eps;
+  }
   if (grid > INT32_MAX) return cudaErrorInvalidValue;
   const size_t smem = gemv_smem_bytes<R, W, KS, MT>(KC);
   static_assert(!NORM || (MT == 1 && !SWIGLU), "the RMSNorm prologue is one-token, single-output");
-  auto kern = q4k_gemv_kernel<R, W, KS, SWIGLU, MT, NORM>;
+  auto kern = q4k_gemv_kernel<R, W, KS, SWIGLU, MT, NORM, ROPE>;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -641,11 +738,22 @@ cudaError_t launch_gemv_cfg(const GemvJob& job, cudaStream_t stream, bool pdl, i
   cfg.blockDim = dim3(W * 32);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  unsigned na = 0;
+  if (pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  if (ROPE) {  // the CTAs of one head form a cluster
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = kRopeCluster;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
+  cfg.numAttrs = na;
   const int pre = (W * pre_pct + 99) / 100;
   return cudaLaunchKernelEx(&cfg, kern, b, static_cast<const uint8_t*>(job.w1), static_cast<const __half*>(job.x),
                             NB, KC, trigger, pre, job.M, job.out_f16, job.gamma, job.eps);
@@ -760,6 +868,29 @@ cudaError_t launch_gemv_batch_rmsnorm(const void* const* w, void* const* y, cons
   job.eps = eps;
   return run_gemv(job, stream);
 }
+
+cudaError_t launch_gemv_qkv_rope(const void* const* w, void* const* y, const int64_t* N, int n_rope,
+                                 const float* const* head_gamma, float head_eps, int pos, double rope_base,
+                                 const void* x, const float* gamma, float eps, int64_t K, cudaStream_t stream) {
+  if (n_rope < 1 || n_rope > 2) return cudaErrorInvalidValue;
+  GemvJob job{w, y, N, 3, nullptr, x, K, 1, 0};
+  job.gamma = gamma;
+  job.eps = eps;
+  job.rope_mask = (1u << n_rope) - 1u;
+  for (int i = 0; i < n_rope; ++i) job.hgamma[i] = head_gamma[i];
+  job.rope_pos = pos;
+  job.rope_log2_base = log2(rope_base);
+  job.head_eps = head_eps;
+  const DevInfo& dev = device_info();
+  const Knobs& kn = knobs();
+  if (gamma != nullptr)
+    return launch_gemv_cfg<1, 4, 1, false, 1, true, true>(job, stream, dev.pdl, kn.trigger, kn.pre_pct);
+  return launch_gemv_cfg<1, 4, 1, false, 1, false, true>(job, stream, dev.pdl, kn.trigger, kn.pre_pct);
+}
+
+#ifdef JLLM_FAULT_INJECTION
+cudaError_t fault_injection_set_gemv(int skip_w) { return cudaMemcpyToSymbol(g_fi_skip_w, &skip_w, sizeof(int)); }
+#endif
 
 cudaError_t read_clear_gemv_error(uint32_t* bits) {
   uint32_t v = 0;

@@ -40,6 +40,16 @@ cudaError_t launch_gemv_batch(const void* const* w, void* const* y, const int64_
 cudaError_t launch_gemv_batch_rmsnorm(const void* const* w, void* const* y, const int64_t* N, int count,
                                       const void* x, const float* gamma, float eps, int64_t K, cudaStream_t s);
 
+// The q/k/v GEMVs of an attention block in one launch (w, y: 3 matrices
+// over the same x, M = 1, fp32 outputs) with a rotary epilogue on the first
+// n_rope (1 or 2) matrices: heads of 128 rows, optional per-head RMSNorm
+// (head_gamma[i] [128] or nullptr), rotation by pos * base^(-2j/128) of
+// pairs (j, j + 64).  gamma != nullptr adds the RMSNorm prologue on x.
+// Every N[i] must be a multiple of 128.
+cudaError_t launch_gemv_qkv_rope(const void* const* w, void* const* y, const int64_t* N, int n_rope,
+                                 const float* const* head_gamma, float head_eps, int pos, double rope_base,
+                                 const void* x, const float* gamma, float eps, int64_t K, cudaStream_t s);
+
 // TMA + tcgen05 GEMM for any M >= 1.  w1 != nullptr selects the SwiGLU
 // epilogue (y = fp16 h).  ws (nullptr allowed) of at least
 // gemm_workspace_bytes() zero-initialised bytes enables the stream-K split.
@@ -64,6 +74,12 @@ cudaError_t gemm_static_workspace(void** ptr, size_t* bytes);
 // Zero the stream-K flag words of the static workspace on the current device
 // (enqueued on s, then s is synchronised); a no-op if it was never used.
 cudaError_t gemm_static_workspace_reset(cudaStream_t s);
+
+#ifdef JLLM_FAULT_INJECTION
+// Test builds only: make one bounded wait of the next launches run out.
+cudaError_t fault_injection_set_gemm(int skip_x);
+cudaError_t fault_injection_set_gemv(int skip_w);
+#endif
 
 // Read and clear the device error word of the tcgen05 kernels (after
 // synchronising the stream) and of the GEMV kernels.

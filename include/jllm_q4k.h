@@ -153,6 +153,40 @@ jllm_status jllm_q4k_gemv_rmsnorm_batch(const void* const* w_q4k, float* const* 
                                         int64_t K, jllm_stream_t stream);
 
 /*
+ * jllm_q4k_gemv_qkv_rope -- the q, k and v projections of one decode token in
+ * one launch, with the rotary position embedding applied to q and k in the
+ * epilogue: the RoPE of the README's "fused RMSNorm + RoPE + SwiGLU" kernel
+ * (At a glance, Kernels bullet).  The pages print no rotary formula; this is
+ * the form of the Qwen3 model they run:
+ *   xn     = x, or the RMSNorm of x when gamma != NULL (as in
+ *            jllm_q4k_gemv_rmsnorm_batch)
+ *   q, k   = dequant(Wq) xn, dequant(Wk) xn; v = dequant(Wv) xn
+ *   per head h of q (and of k), 128 values t[0..127]:
+ *     optional per-head RMSNorm: t = t * g / sqrt(sum(t^2)/128 + head_eps),
+ *       g = q_gamma (resp. k_gamma) [128], skipped when that pointer is NULL
+ *     rotation of pairs (j, j+64), j < 64, by a = pos * rope_base^(-2j/128):
+ *       out[j] = t[j] cos a - t[j+64] sin a;  out[j+64] = t[j+64] cos a + t[j] sin a
+ *   w_q4k : host array of 3 device pointers: Wq [n_q_heads*128][K/256]
+ *           blocks, Wk and Wv [n_kv_heads*128][K/256] blocks
+ *   y     : host array of 3 device pointers: q [n_q_heads*128], k and v
+ *           [n_kv_heads*128], fp32 (q, k rotated; v plain)
+ *   x     : [K] fp16; gamma: [K] fp32 or NULL, eps in [0, 1]
+ *   q_gamma, k_gamma: [128] fp32 or NULL; head_eps in [0, 1]
+ *   pos   : token position (any 32-bit value); rope_base > 0 (Qwen3: 1e6)
+ * Head size 128 only.  The angle is formed in fp64 and its cosine and sine
+ * rounded to fp32; each q/k value stays within the matmul bound propagated
+ * through the norm and the rotation.  The 8 CTAs that compute one head form
+ * a thread-block cluster and reduce the head's sum of squares through
+ * distributed shared memory.  gamma, q_gamma and k_gamma, like the weights,
+ * must not be written by the kernel enqueued just before (PDL paragraph).
+ * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED, CUDA.
+ */
+jllm_status jllm_q4k_gemv_qkv_rope(const void* const* w_q4k, float* const* y, int64_t n_q_heads,
+                                   int64_t n_kv_heads, const void* x, int64_t K, const float* gamma,
+                                   float eps, const float* q_gamma, const float* k_gamma, float head_eps,
+                                   int64_t pos, float rope_base, jllm_stream_t stream);
+
+/*
  * jllm_q4k_gemm -- Y[M,N] = X[M,K] * dequant(W)^T for any M >= 1.
  * (the README's "tensor-core MMQ Q4_K prefill" for M above the GEMV
  *  threshold, the GEMV kernel at or below it)
