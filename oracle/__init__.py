@@ -23,6 +23,9 @@ Every function restates a definition in plain single-threaded C, fp64:
   angle pos * base^(-2i/D)), the RoPE of the same kernel bullet; the pages
   print no formula, this is the form of the Qwen3 model they run.
   ``head_rmsnorm`` -- ``rmsnorm`` applied per head vector (Qwen3's q/k norm).
+* ``kv_encode`` / ``kv_decode`` -- the FP16 <-> INT8 KV codec of the README's KV
+  cache bullet (per-vector power-of-two scale, round half to even; the rule and
+  why it is drift-free are in q4k_oracle.c; the pages give no granularity).
 * ``quantize`` -- a plain non-iterative quantiser used only for the round-trip
   pin (not on the pages; the rule is stated in q4k_oracle.c).
 
@@ -85,6 +88,10 @@ def _load():
     lib.oq_rmsnorm.restype = None
     lib.oq_rope.argtypes = [P, I64, I64, I64, ctypes.c_double, P]
     lib.oq_rope.restype = None
+    lib.oq_kv_encode.argtypes = [P, I64, I64, P, P]
+    lib.oq_kv_encode.restype = None
+    lib.oq_kv_decode.argtypes = [P, P, I64, I64, P]
+    lib.oq_kv_decode.restype = None
     lib.oq_quantize_block.argtypes = [P, P]
     lib.oq_quantize_block.restype = None
     lib.oq_quantize.argtypes = [P, I64, I64, P]
@@ -234,6 +241,31 @@ def head_rmsnorm(v: np.ndarray, gamma: np.ndarray, eps: float, head_dim: int = 1
     RoPE): ``rmsnorm`` on v viewed as [heads, head_dim] rows, gamma [head_dim]."""
     va = np.asarray(v, dtype=np.float64)
     return rmsnorm(va.reshape(-1, head_dim), gamma, eps).reshape(va.shape)
+
+
+def kv_encode(v: np.ndarray, dim: int = 128) -> tuple[np.ndarray, np.ndarray]:
+    """INT8 KV codec: fp16 vectors of `dim` values -> (int8 codes [..., dim], fp16 power-of-two
+    scales [...]); see oq_kv_encode for the rule."""
+    va = np.ascontiguousarray(np.asarray(v, dtype=np.float16))
+    if va.size % dim:
+        raise ValueError("size must be a multiple of dim")
+    n = va.size // dim
+    q = np.empty(va.shape, dtype=np.int8)
+    sc = np.empty(n, dtype=np.uint16)
+    _load().oq_kv_encode(_ptr(va.view(np.uint16)), n, dim, _ptr(q), _ptr(sc))
+    return q, sc.view(np.float16).reshape(va.shape[:-1] if va.ndim > 1 and va.shape[-1] == dim else (n,))
+
+
+def kv_decode(q: np.ndarray, scales: np.ndarray, dim: int = 128) -> np.ndarray:
+    """INT8 KV codec: codes and scales -> fp16 values q * scale."""
+    qa = np.ascontiguousarray(np.asarray(q, dtype=np.int8))
+    sa = np.ascontiguousarray(np.asarray(scales, dtype=np.float16)).view(np.uint16)
+    n = qa.size // dim
+    if qa.size % dim or sa.size != n:
+        raise ValueError("one scale per vector of dim codes")
+    out = np.empty(qa.shape, dtype=np.uint16)
+    _load().oq_kv_decode(_ptr(qa), _ptr(sa), n, dim, _ptr(out))
+    return out.view(np.float16)
 
 
 def quantize(w: np.ndarray) -> np.ndarray:

@@ -272,6 +272,55 @@ void oq_rope(const double* v, int64_t n_heads, int64_t head_dim, int64_t pos, do
   }
 }
 
+/* ------------------------------------------------------- INT8 KV codec --- */
+
+/* The "FP16 <-> INT8 KV convert" of the README (At a glance, KV cache bullet:
+ * INT8 by default with "FP16-ULP-bounded drift"; Project layout, src/kernels/).
+ * The pages give neither the scale granularity nor the rounding.  Reading:
+ * one scale per vector of `dim` fp16 values (one head of one token), symmetric,
+ * the scale a power of two s = 2^e stored as fp16:
+ *   amax = max |v|;  e = the smallest integer with amax <= 127 * 2^e, clamped
+ *   to [-24, 9] (e = -24 also for amax = 0);
+ *   q = round-half-even(v / 2^e), clamped to [-127, 127];  decode v' = q * 2^e.
+ * q * 2^e is exactly representable in fp16 for every such e and q, so decode is
+ * exact and encode(decode(encode(v))) == encode(v): a second round trip does
+ * not move any value (no drift at all, the strongest form of a drift bound).
+ * The round trip moves each value by at most 2^e / 2 (2^e once the code
+ * saturates, which only happens for amax above 127.5 * 2^9 = 65280). */
+static int kv_exponent(double amax) {
+  int e = -24;
+  while (e < 9 && amax > 127.0 * ldexp(1.0, e)) e++;
+  return e;
+}
+
+void oq_kv_encode(const uint16_t* v, int64_t n_vec, int64_t dim, int8_t* q, uint16_t* scale) {
+  for (int64_t i = 0; i < n_vec; i++) {
+    const uint16_t* vi = v + i * dim;
+    double amax = 0.0;
+    for (int64_t k = 0; k < dim; k++) {
+      double a = fabs(oq_half_to_double(vi[k]));
+      if (a > amax) amax = a;
+    }
+    const int e = kv_exponent(amax);
+    const double s = ldexp(1.0, e);
+    for (int64_t k = 0; k < dim; k++) {
+      double t = oq_half_to_double(vi[k]) / s; /* exact: a power-of-two scaling */
+      double r = nearbyint(t);                 /* round half to even (default mode) */
+      if (r > 127.0) r = 127.0;
+      if (r < -127.0) r = -127.0;
+      q[i * dim + k] = (int8_t)r;
+    }
+    scale[i] = oq_float_to_half_rne((float)s); /* 2^e, exact in fp16 */
+  }
+}
+
+void oq_kv_decode(const int8_t* q, const uint16_t* scale, int64_t n_vec, int64_t dim, uint16_t* out) {
+  for (int64_t i = 0; i < n_vec; i++) {
+    const double s = oq_half_to_double(scale[i]);
+    for (int64_t k = 0; k < dim; k++) out[i * dim + k] = oq_float_to_half_rne((float)((double)q[i * dim + k] * s));
+  }
+}
+
 /* ------------------------------------------------------------ quantiser --- */
 
 /* Smallest binary16 value >= v (v >= 0, finite, below 65504), as bits. */

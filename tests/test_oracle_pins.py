@@ -443,6 +443,80 @@ def test_head_rmsnorm_is_rmsnorm_per_head():
         assert np.mean((hn[h] / g) ** 2) == pytest.approx(1.0, rel=1e-5)
 
 
+# ---------------------------------------------------------- INT8 KV codec ----
+
+def _kv_vectors(rng, n, dim=128):
+    """fp16 vectors over many magnitudes, with some subnormal-only and some near the top of fp16."""
+    mag = 10.0 ** rng.uniform(-9, 4.5, size=(n, 1))
+    v = np.clip(rng.standard_normal((n, dim)) * mag, -65504, 65504)
+    return v.astype(np.float16)
+
+
+def test_kv_scale_is_the_smallest_power_of_two_covering_the_vector():
+    rng = np.random.Generator(np.random.PCG64(90))
+    v = _kv_vectors(rng, 3000)
+    q, s = oracle.kv_encode(v)
+    amax = np.max(np.abs(v.astype(np.float64)), axis=1)
+    for i in range(v.shape[0]):
+        # brute force over every allowed exponent
+        cands = [e for e in range(-24, 10) if amax[i] <= 127.0 * 2.0**e]
+        e = cands[0] if cands else 9
+        assert float(s[i]) == 2.0**e, (i, amax[i], float(s[i]))
+    # unclamped vectors use codes up to 127 and at least 64 in magnitude
+    inner = (amax > 127.0 * 2.0**-24) & (amax <= 127.0 * 2.0**9)
+    qmax = np.max(np.abs(q.astype(np.int64)), axis=1)
+    assert np.all((qmax[inner] >= 64) & (qmax[inner] <= 127))
+
+
+def test_kv_closed_forms():
+    # exact multiples of the scale come back exactly, codes = the multiples
+    k = np.arange(-127, 129, dtype=np.int64)[:128]
+    for e in (-24, -20, -3, 0, 5, 9):
+        v = (k * 2.0**e).astype(np.float16)
+        q, s = oracle.kv_encode(v[None, :])
+        assert float(s[0]) == 2.0**e and np.array_equal(q[0].astype(np.int64), k)
+        assert np.array_equal(oracle.kv_decode(q, s), v[None, :])
+    # round half to even: 2.5 -> 2, 3.5 -> 4, -0.5 -> -0, with the scale pinned to 1 by 127
+    v = np.zeros(128, dtype=np.float16)
+    v[:4] = [127.0, 2.5, 3.5, -0.5]
+    q, s = oracle.kv_encode(v[None, :])
+    assert float(s[0]) == 1.0 and list(q[0, :4]) == [127, 2, 4, 0]
+    # a zero vector stays zero; sign symmetry
+    q0, s0 = oracle.kv_encode(np.zeros((1, 128), np.float16))
+    assert not q0.any() and np.all(oracle.kv_decode(q0, s0) == 0)
+    rng = np.random.Generator(np.random.PCG64(91))
+    v = _kv_vectors(rng, 200)
+    qa, sa = oracle.kv_encode(v)
+    qb, sb = oracle.kv_encode(-v)
+    assert np.array_equal(qb, -qa) and np.array_equal(sb, sa)
+    # the top of the fp16 range saturates: 65504 / 512 = 127.94 -> 127, decoded 65024
+    v = np.zeros((1, 128), np.float16)
+    v[0, 0] = 65504.0
+    q, s = oracle.kv_encode(v)
+    assert float(s[0]) == 512.0 and q[0, 0] == 127 and float(oracle.kv_decode(q, s)[0, 0]) == 65024.0
+
+
+def test_kv_round_trip_error_and_no_drift():
+    rng = np.random.Generator(np.random.PCG64(92))
+    v = _kv_vectors(rng, 4000)
+    q, s = oracle.kv_encode(v)
+    d = oracle.kv_decode(q, s)
+    err = np.abs(d.astype(np.float64) - v.astype(np.float64))
+    sf = s.astype(np.float64)[:, None]
+    amax = np.max(np.abs(v.astype(np.float64)), axis=1)
+    sat = (amax > 127.5 * 2.0**9)[:, None]
+    assert np.all(err <= np.where(sat, sf, sf / 2))
+    # decode is exact (q * 2^e in fp16) and a second round trip changes nothing
+    assert np.array_equal(d.astype(np.float64), q.astype(np.float64) * sf)
+    q2, s2 = oracle.kv_encode(d)
+    assert np.array_equal(q2, q) and np.array_equal(s2, s)
+    assert np.array_equal(oracle.kv_decode(q2, s2), d)
+    # vectors whose values are all below 127 * 2^-24 (fp16 subnormal range) round-trip exactly
+    tiny = (rng.integers(-127, 128, size=(50, 128)) * 2.0**-24).astype(np.float16)
+    qt, st = oracle.kv_encode(tiny)
+    assert np.all(st.astype(np.float64) == 2.0**-24) and np.array_equal(oracle.kv_decode(qt, st), tiny)
+
+
 def test_synthetic_weights_distribution():
     w = synthetic.q4k_weights(64, 2560, seed=1)
     assert w.shape == (64, 10 * 144)
