@@ -38,30 +38,36 @@ def _newest_input() -> float:
     return max(os.path.getmtime(f) for f in files)
 
 
-def _up_to_date() -> bool:
-    return os.path.exists(LIB) and os.path.getmtime(LIB) >= _newest_input()
+def _up_to_date(lib: str) -> bool:
+    return os.path.exists(lib) and os.path.getmtime(lib) >= _newest_input()
 
 
-def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None) -> str:
+def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None, variant: str = "") -> str:
     """Compile the library if it is missing or older than its sources; return its path.
     Processes that build at the same time (the ranks of one job) take turns on a lock
-    file, and a process that waited finds the library already built."""
-    if not force and _up_to_date():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
-    with open(os.path.join(BUILD, ".lock"), "w") as lock:
+    file, and a process that waited finds the library already built.
+
+    variant: a named build with extra compiler flags (`extra`), kept apart from the
+    shipped library (its objects in _build_<variant>/, the library in
+    libjllm_q4k_<variant>.so); the tests use one with -DJLLM_FAULT_INJECTION."""
+    lib = LIB if not variant else os.path.join(PKG, f"libjllm_q4k_{variant}.so")
+    bdir = BUILD if not variant else os.path.join(PKG, f"_build_{variant}")
+    if not force and _up_to_date(lib):
+        return lib
+    os.makedirs(bdir, exist_ok=True)
+    with open(os.path.join(bdir, ".lock"), "w") as lock:
         fcntl.flock(lock, fcntl.LOCK_EX)
-        if not force and _up_to_date():
-            return LIB
-        return _build_locked(verbose, extra)
+        if not force and _up_to_date(lib):
+            return lib
+        return _build_locked(verbose, extra, lib, bdir)
 
 
-def _build_locked(verbose: bool, extra: list[str] | None) -> str:
+def _build_locked(verbose: bool, extra: list[str] | None, lib: str, bdir: str) -> str:
     nvcc = _nvcc()
     flags = ARCH + CFLAGS + (extra or [])
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(bdir, os.path.basename(src)[:-3] + ".o")
         cmd = [nvcc, *flags, "-c", src, "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
@@ -74,12 +80,12 @@ def _build_locked(verbose: bool, extra: list[str] | None) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 1)) as ex:
         objs = list(ex.map(compile_one, sources()))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     res = subprocess.run([nvcc, *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{res.stdout}\n{res.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -1,0 +1,99 @@
+"""The bounded-wait error path, exercised on the GPU without a fault.
+
+A test build of the library (-DJLLM_FAULT_INJECTION, waits limited to 20 ms)
+has a switch that makes one copy never be issued: CTA 0 of the tcgen05 GEMM
+skips its first X tile, or warp 0 of CTA 0 of the GEMV skips its weight
+rows.  The wait on that copy then runs out: the kernel must set its error
+word, wind down (copies and MMAs in flight awaited, tensor memory freed) and
+return, jllm_get_device_error must report JLLM_ERR_DEVICE_TIMEOUT, and the
+next calls on the same context must be correct again -- including
+jllm_q4k_gemm_noalloc, whose static workspace a timed-out call leaves with
+stale stream-K flags until jllm_get_device_error clears them.  Runs in a child
+process so that the test library is the only one loaded there."""
+import os
+import subprocess
+import sys
+
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+CHILD = r'''
+import ctypes, sys, time
+import numpy as np, torch
+root, lib_path = sys.argv[1], sys.argv[2]
+sys.path.insert(0, root); sys.path.insert(0, root + "/tests")
+import oracle, synthetic
+lib = ctypes.CDLL(lib_path)
+P, I64 = ctypes.c_void_p, ctypes.c_int64
+lib.jllm_q4k_gemm_noalloc.argtypes = [P, P, P, ctypes.c_int, I64, I64, I64, P]
+lib.jllm_q4k_gemm.argtypes = [P, P, P, ctypes.c_int, I64, I64, I64, P, ctypes.c_size_t, P]
+lib.jllm_q4k_gemv.argtypes = [P, P, P, I64, I64, P, ctypes.c_size_t, P]
+lib.jllm_q4k_workspace_bytes.argtypes = [I64, I64, I64]
+lib.jllm_q4k_workspace_bytes.restype = ctypes.c_size_t
+lib.jllm_get_device_error.argtypes = [P]
+lib.jllm_test_fault_injection.argtypes = [ctypes.c_int, ctypes.c_int]
+TIMEOUT = 7
+s = torch.cuda.current_stream().cuda_stream
+
+def within(y, ref, s_):
+    return bool(np.all(np.abs(y.astype(np.float64) - ref) <= oracle.tolerance(s_)))
+
+# tcgen05 GEMM with the stream-K split: 16 tiles over 80 CTAs, CTA 0 finishes tile 0
+M, N, K = 235, 1024, 2560
+w = synthetic.q4k_weights(N, K, 9500); x = synthetic.activations(M, K, 9501)
+ref, sref = oracle.matmul(w, x, N, K)
+wd, xd = torch.from_numpy(w).cuda(), torch.from_numpy(x).cuda()
+y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+noalloc = lambda: lib.jllm_q4k_gemm_noalloc(wd.data_ptr(), xd.data_ptr(), y.data_ptr(), 0, M, N, K, s)
+assert noalloc() == 0 and lib.jllm_get_device_error(s) == 0 and within(y.cpu().numpy(), ref, sref)
+for rnd in range(2):
+    assert lib.jllm_test_fault_injection(1, 0) == 0
+    t0 = time.time()
+    assert noalloc() == 0
+    st = lib.jllm_get_device_error(s)
+    assert st == TIMEOUT, st
+    assert time.time() - t0 < 5.0  # the kernel returned after its bounded waits
+    assert lib.jllm_test_fault_injection(0, 0) == 0
+    for _ in range(2):
+        y.fill_(float("nan"))
+        assert noalloc() == 0
+        assert lib.jllm_get_device_error(s) == 0
+        assert within(y.cpu().numpy(), ref, sref), "noalloc after a timeout"
+
+# the same with a caller workspace: zero-filled again by its owner after the timeout
+need = lib.jllm_q4k_workspace_bytes(M, N, K)
+ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+gemm = lambda: lib.jllm_q4k_gemm(wd.data_ptr(), xd.data_ptr(), y.data_ptr(), 0, M, N, K, ws.data_ptr(), need, s)
+assert lib.jllm_test_fault_injection(1, 0) == 0
+assert gemm() == 0 and lib.jllm_get_device_error(s) == TIMEOUT
+assert lib.jllm_test_fault_injection(0, 0) == 0
+ws.zero_()
+assert gemm() == 0 and lib.jllm_get_device_error(s) == 0 and within(y.cpu().numpy(), ref, sref)
+
+# GEMV (M = 1): warp 0 of CTA 0 never gets its rows
+N1 = 4096
+w1 = synthetic.q4k_weights(N1, K, 9502); x1 = synthetic.activations(1, K, 9503)
+r1, s1 = oracle.matmul(w1, x1, N1, K)
+w1d, x1d = torch.from_numpy(w1).cuda(), torch.from_numpy(x1.reshape(K)).cuda()
+y1 = torch.empty(N1, dtype=torch.float32, device="cuda")
+gemv = lambda: lib.jllm_q4k_gemv(w1d.data_ptr(), x1d.data_ptr(), y1.data_ptr(), N1, K, None, 0, s)
+assert lib.jllm_test_fault_injection(0, 1) == 0
+assert gemv() == 0 and lib.jllm_get_device_error(s) == TIMEOUT
+assert lib.jllm_test_fault_injection(0, 0) == 0
+assert gemv() == 0 and lib.jllm_get_device_error(s) == 0 and within(y1.cpu().numpy()[None, :], r1, s1)
+print("ok")
+'''
+
+
+def test_bounded_waits_report_timeout_and_recover():
+    import importlib.util
+
+    spec = importlib.util.spec_from_file_location("_jllm_build", os.path.join(ROOT, "bit_q4_weight_gb300", "_build.py"))
+    b = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(b)
+    lib = b.build(variant="fi", extra=["-DJLLM_FAULT_INJECTION", "-DJLLM_WAIT_LIMIT_NS=20000000ull"])
+    out = subprocess.run([sys.executable, "-c", CHILD, ROOT, lib], capture_output=True, text=True, timeout=900)
+    assert out.returncode == 0 and out.stdout.strip().endswith("ok"), (out.stdout[-2000:], out.stderr[-3000:])
