@@ -46,6 +46,8 @@ EXPORTS = (
     "jllm_q4k_gemm_noalloc",
     "jllm_q4k_gemm_batch",
     "jllm_q4k_ffn_swiglu",
+    "jllm_kv_encode_i8",
+    "jllm_kv_decode_i8",
     "jllm_q4k_workspace_bytes",
     "jllm_q4k_gemv_max_m",
     "jllm_get_device_error",
@@ -90,6 +92,10 @@ lib.jllm_q4k_gemm_batch.argtypes = [_P, _P, _P, ctypes.c_int, _I64, _P, _I64, ct
 lib.jllm_q4k_gemm_batch.restype = _ST
 lib.jllm_q4k_ffn_swiglu.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P]
 lib.jllm_q4k_ffn_swiglu.restype = _ST
+lib.jllm_kv_encode_i8.argtypes = [_P, _P, _P, _I64, _I64, _P]
+lib.jllm_kv_encode_i8.restype = _ST
+lib.jllm_kv_decode_i8.argtypes = [_P, _P, _P, _I64, _I64, _P]
+lib.jllm_kv_decode_i8.restype = _ST
 lib.jllm_q4k_workspace_bytes.argtypes = [_I64, _I64, _I64]
 lib.jllm_q4k_workspace_bytes.restype = _SZ
 lib.jllm_q4k_gemv_max_m.argtypes = []
@@ -376,6 +382,40 @@ def jllm_q4k_gemm_batch(ws_q4k, x, Ns, K: int, out_dtype=None, outs=None, ws=Non
         "jllm_q4k_gemm_batch",
     )
     return outs
+
+
+def jllm_kv_encode_i8(kv, head_dim: int = 128, codes=None, scales=None, stream=None):
+    """fp16 KV vectors [..., head_dim] -> (int8 codes of the same shape, fp16 scales [...])."""
+    torch = _torch()
+    if kv.shape[-1] != head_dim:
+        raise ValueError("last dimension must be head_dim")
+    _need(kv, torch.float16, None, "kv")
+    n = kv.numel() // head_dim
+    if codes is None:
+        codes = torch.empty(kv.shape, dtype=torch.int8, device=kv.device)
+    if scales is None:
+        scales = torch.empty(kv.shape[:-1], dtype=torch.float16, device=kv.device)
+    _need(codes, torch.int8, kv.shape, "codes")
+    _need(scales, torch.float16, kv.shape[:-1], "scales")
+    _check(lib.jllm_kv_encode_i8(kv.data_ptr(), codes.data_ptr(), scales.data_ptr(), n, head_dim, _stream_ptr(stream)),
+           "jllm_kv_encode_i8")
+    return codes, scales
+
+
+def jllm_kv_decode_i8(codes, scales, head_dim: int = 128, out=None, stream=None):
+    """int8 codes [..., head_dim] and fp16 scales [...] -> fp16 KV vectors."""
+    torch = _torch()
+    if codes.shape[-1] != head_dim:
+        raise ValueError("last dimension must be head_dim")
+    _need(codes, torch.int8, None, "codes")
+    _need(scales, torch.float16, codes.shape[:-1], "scales")
+    n = codes.numel() // head_dim
+    if out is None:
+        out = torch.empty(codes.shape, dtype=torch.float16, device=codes.device)
+    _need(out, torch.float16, codes.shape, "out")
+    _check(lib.jllm_kv_decode_i8(codes.data_ptr(), scales.data_ptr(), out.data_ptr(), n, head_dim, _stream_ptr(stream)),
+           "jllm_kv_decode_i8")
+    return out
 
 
 def jllm_q4k_ffn_swiglu(w_gate, w_up, x, N: int, K: int, out=None, ws=None, stream=None):

@@ -294,6 +294,29 @@ jllm_status jllm_q4k_ffn_swiglu(const void* w_gate, const void* w_up, const void
   return from_cuda(jllm::launch_gemm_tc(w_gate, w_up, x, h, true, M, N, K, ws, ws_bytes, s));
 }
 
+static jllm_status check_kv(const void* a, const void* b, const void* scales, int64_t n_vectors, int64_t head_dim) {
+  if (!a || !b || !scales) return JLLM_ERR_INVALID_ARG;
+  if (n_vectors < 1) return JLLM_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128 && head_dim != 256) return JLLM_ERR_UNSUPPORTED_SHAPE;
+  if (n_vectors > ((int64_t)1 << 40) / head_dim) return JLLM_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(a) || !aligned16(b) || ((uintptr_t)scales & 1u)) return JLLM_ERR_MISALIGNED;
+  return check_device();
+}
+
+jllm_status jllm_kv_encode_i8(const void* kv, int8_t* codes, void* scales, int64_t n_vectors, int64_t head_dim,
+                              jllm_stream_t stream) {
+  jllm_status st = check_kv(kv, codes, scales, n_vectors, head_dim);
+  if (st != JLLM_OK) return st;
+  return from_cuda(jllm::launch_kv_encode(kv, codes, scales, n_vectors, (int)head_dim, (cudaStream_t)stream));
+}
+
+jllm_status jllm_kv_decode_i8(const int8_t* codes, const void* scales, void* kv, int64_t n_vectors, int64_t head_dim,
+                              jllm_stream_t stream) {
+  jllm_status st = check_kv(codes, kv, scales, n_vectors, head_dim);
+  if (st != JLLM_OK) return st;
+  return from_cuda(jllm::launch_kv_decode(codes, scales, kv, n_vectors, (int)head_dim, (cudaStream_t)stream));
+}
+
 jllm_status jllm_get_device_error(jllm_stream_t stream) {
   uint32_t a = 0, b = 0;
   cudaError_t e = jllm::read_clear_gemm_error(&a, (cudaStream_t)stream);

@@ -63,6 +63,11 @@ constexpr int kMaxGemmBatch = 4;
 cudaError_t launch_gemm_tc_batch(const void* const* w, const int64_t* N, int count, const void* x, void* const* y,
                                  bool y_f16, int64_t M, int64_t K, void* ws, size_t ws_bytes, cudaStream_t s);
 
+// FP16 <-> INT8 KV codec over n_vec vectors of dim (64, 128 or 256) values:
+// codes [n_vec][dim] int8, one fp16 power-of-two scale per vector.
+cudaError_t launch_kv_encode(const void* kv, int8_t* codes, void* scales, int64_t n_vec, int dim, cudaStream_t s);
+cudaError_t launch_kv_decode(const int8_t* codes, const void* scales, void* kv, int64_t n_vec, int dim, cudaStream_t s);
+
 // Workspace of the stream-K split on the current device: one 128 KiB fp32
 // partial slot and one flag word per SM (0 when the device is unusable).
 size_t gemm_workspace_bytes();

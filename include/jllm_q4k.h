@@ -270,6 +270,32 @@ jllm_status jllm_q4k_ffn_swiglu(const void* w_gate, const void* w_up, const void
                                 jllm_stream_t stream);
 
 /*
+ * jllm_kv_encode_i8 / jllm_kv_decode_i8 -- the FP16 <-> INT8 KV cache codec
+ * (the README's "FP16<->INT8 KV convert" kernel, Project layout, src/kernels/;
+ * At a glance, KV cache bullet: "INT8 by default", "FP16-ULP-bounded drift").
+ * The pages give no scale granularity or rounding; this library's rule: one
+ * scale per vector of head_dim values (one head of one token), symmetric, a
+ * power of two s = 2^e stored as fp16, e the smallest integer with
+ * max|v| <= 127 * 2^e clamped to [-24, 9];
+ *   encode: q = round-half-even(v / s) clamped to [-127, 127]
+ *   decode: v' = q * s (exact in fp16)
+ * so |v' - v| <= s/2 (<= s where the code saturates, max|v| > 65280), and
+ * decode(encode(decode(encode(v)))) == decode(encode(v)) bit for bit: the
+ * codec does not drift under repeated round trips.  Codes and scales are
+ * bit-exact to that rule for finite inputs (non-finite values give
+ * unspecified codes).
+ *   kv      : [n_vectors][head_dim] fp16, 16-byte aligned
+ *   codes   : [n_vectors][head_dim] int8, 16-byte aligned
+ *   scales  : [n_vectors] fp16, 2-byte aligned
+ *   head_dim: 64, 128 or 256
+ * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED, CUDA.
+ */
+jllm_status jllm_kv_encode_i8(const void* kv, int8_t* codes, void* scales, int64_t n_vectors, int64_t head_dim,
+                              jllm_stream_t stream);
+jllm_status jllm_kv_decode_i8(const int8_t* codes, const void* scales, void* kv, int64_t n_vectors,
+                              int64_t head_dim, jllm_stream_t stream);
+
+/*
  * Workspace bytes that gemm/ffn_swiglu can use for this shape on the current
  * device (0 = the call takes none).  Passing ws = NULL is always allowed and
  * only gives up the stream-K split.  A workspace that is given must be at
