@@ -88,6 +88,21 @@ def _build_locked(verbose: bool, extra: list[str] | None, lib: str, bdir: str) -
     return lib
 
 
+def build_microbench() -> str:
+    """Compile microbench/tc_rates.cu (tensor-core rate measurements, not part of the library)
+    into its own shared object; return its path."""
+    src = os.path.join(PKG, "microbench", "tc_rates.cu")
+    lib = os.path.join(PKG, "microbench", "libjllm_microbench.so")
+    if os.path.exists(lib) and os.path.getmtime(lib) >= max(os.path.getmtime(src), _newest_input()):
+        return lib
+    tmp = lib + f".tmp{os.getpid()}"
+    res = subprocess.run([_nvcc(), *ARCH, *CFLAGS, "-shared", src, "-o", tmp], capture_output=True, text=True)
+    if res.returncode != 0:
+        raise RuntimeError(f"nvcc failed for {src}:\n{res.stdout}\n{res.stderr}")
+    os.replace(tmp, lib)
+    return lib
+
+
 if __name__ == "__main__":
     import sys
 

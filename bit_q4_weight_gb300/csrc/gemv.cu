@@ -223,12 +223,12 @@ struct GemvBatch {
   // Rotary epilogue (ROPE kernels): matrix i with bit i of rope_mask set holds
   // heads of 128 rows; hgamma[i] is its per-head RMSNorm weight [128]
   // (nullptr: no per-head norm).  Angle of pair j at position pos:
-  // pos * 2^(-(j/64) * log2_base).
+  // pos * rope_theta[j], rope_theta[j] = base^(-2j/128) formed on the host in fp64.
   const float* hgamma[kMaxGemvBatch];
   unsigned rope_mask;
   int rope_pos;
-  double rope_log2_base;
   float head_eps;
+  double rope_theta[64];
 };
 
 constexpr int kHeadDim = 128;     // rows per head in the rotary epilogue
@@ -592,10 +592,14 @@ __global__ void __launch_bounds__(W * 32, 512 / (W * 32)) q4k_gemv_kernel(const 
         a = __fmul_rn(__fmul_rn(a, r), hgamma[j]);
         b = __fmul_rn(__fmul_rn(b, r), hgamma[j + kHeadDim / 2]);
       }
-      // angle pos * base^(-2j/128) in fp64 (exact enough at any position), then fp32
-      double sd, cd;
-      sincos((double)batch.rope_pos * exp2(-(double)j / (kHeadDim / 2) * batch.rope_log2_base), &sd, &cd);
-      const float c = (float)cd, sn = (float)sd;
+      // angle pos * theta_j and its reduction modulo 2 pi in fp64 (pi split in two parts, so
+      // the remainder stays accurate at any 32-bit position), sine and cosine in fp32
+      const double ang = (double)batch.rope_pos * batch.rope_theta[j];
+      const double kq = rint(ang * 0.15915494309189535);           // 1 / (2 pi)
+      double rr = fma(-kq, 6.283185307179586, ang);                  // 2 pi, high part
+      rr = fma(-kq, 2.4492935982947064e-16, rr);                     // 2 pi, low part
+      float sn, c;
+      sincosf((float)rr, &sn, &c);
       float* yo = reinterpret_cast<float*>(y) + (int64_t)(ccta / kRopeCluster) * kHeadDim;
       yo[j] = __fsub_rn(__fmul_rn(a, c), __fmul_rn(b, sn));
       yo[j + kHeadDim / 2] = __fadd_rn(__fmul_rn(b, c), __fmul_rn(a, sn));
@@ -691,7 +695,7 @@ struct GemvJob {
   unsigned rope_mask = 0;
   const float* hgamma[kMaxGemvBatch] = {};
   int rope_pos = 0;
-  double rope_log2_base = 0.0;
+  double rope_base = 0.0;
   float head_eps = 0.f;
 };
 
@@ -722,8 +726,8 @@ cudaError_t launch_gemv_cfg(const GemvJob& job, cudaStream_t stream, bool pdl, i
     }
     b.rope_mask = job.rope_mask;
     b.rope_pos = job.rope_pos;
-    b.rope_log2_base = job.rope_log2_base;
     b.head_eps = job.head_eps;
+    for (int i = 0; i < kHeadDim / 2; ++i) b.rope_theta[i] = pow(job.rope_base, -2.0 * i / kHeadDim);
   }
   if (grid > INT32_MAX) return cudaErrorInvalidValue;
   const size_t smem = gemv_smem_bytes<R, W, KS, MT>(KC);
@@ -879,7 +883,7 @@ cudaError_t launch_gemv_qkv_rope(const void* const* w, void* const* y, const int
   job.rope_mask = (1u << n_rope) - 1u;
   for (int i = 0; i < n_rope; ++i) job.hgamma[i] = head_gamma[i];
   job.rope_pos = pos;
-  job.rope_log2_base = log2(rope_base);
+  job.rope_base = rope_base;
   job.head_eps = head_eps;
   const DevInfo& dev = device_info();
   const Knobs& kn = knobs();

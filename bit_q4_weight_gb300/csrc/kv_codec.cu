@@ -22,15 +22,18 @@ namespace {
 constexpr int KV_THREADS = 256;
 constexpr int KV_UNROLL = 4;
 
+// 2^e as fp32, for the exponents used here (normal range).
+__device__ __forceinline__ float pow2f(int e) { return __int_as_float((e + 127) << 23); }
+
 // Exponent e of the scale for a vector whose largest magnitude is a (finite,
-// >= 0): with a = f * 2^E, f in [0.5, 1), e is E - 7 or E - 6 (127 * 2^(E-7)
-// < 2^E and 127 * 2^(E-6) >= 2^E > a); one exact comparison picks it.
+// >= 0, an fp16 value, so a normal fp32): with a = f * 2^E, f in [0.5, 1), e
+// is E - 7 or E - 6 (127 * 2^(E-7) < 2^E and 127 * 2^(E-6) >= 2^E > a); one
+// exact comparison picks it.
 __device__ __forceinline__ int kv_exponent(float a) {
   if (a == 0.f) return -24;
-  int E;
-  frexpf(a, &E);
+  const int E = ((__float_as_int(a) >> 23) & 0xff) - 126;
   int e = E - 7;
-  if (a > ldexpf(127.f, e)) ++e;
+  if (a > 127.f * pow2f(e)) ++e;
   return e < -24 ? -24 : (e > 9 ? 9 : e);
 }
 
@@ -45,7 +48,7 @@ __device__ __forceinline__ int code_of(float v, float inv) {
 
 // L = lanes per vector (D / 8).
 template <int L>
-__global__ void __launch_bounds__(KV_THREADS) kv_encode_kernel(const uint4* __restrict__ kv, uint2* __restrict__ codes,
+__global__ void __launch_bounds__(KV_THREADS, 5) kv_encode_kernel(const uint4* __restrict__ kv, uint2* __restrict__ codes,
                                                                __half* __restrict__ scales, int64_t n_vec) {
   constexpr int VPW = 32 / L;  // vectors per warp and pass
   const int lane = threadIdx.x & 31, sub = lane % L;
@@ -74,7 +77,7 @@ __global__ void __launch_bounds__(KV_THREADS) kv_encode_kernel(const uint4* __re
 #pragma unroll
       for (int o = L / 2; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
       const int e = kv_exponent(__half2float(__ushort_as_half((unsigned short)m)));
-      const float inv = ldexpf(1.f, -e);
+      const float inv = pow2f(-e);
       if (v < n_vec) {
         const __half2* h = reinterpret_cast<const __half2*>(&u[j]);
         float2 f0 = __half22float2(h[0]), f1 = __half22float2(h[1]), f2 = __half22float2(h[2]), f3 = __half22float2(h[3]);
@@ -82,7 +85,7 @@ __global__ void __launch_bounds__(KV_THREADS) kv_encode_kernel(const uint4* __re
         out.x = pack4_i8(code_of(f0.x, inv), code_of(f0.y, inv), code_of(f1.x, inv), code_of(f1.y, inv));
         out.y = pack4_i8(code_of(f2.x, inv), code_of(f2.y, inv), code_of(f3.x, inv), code_of(f3.y, inv));
         codes[v * L + sub] = out;
-        if (sub == 0) scales[v] = __float2half_rn(ldexpf(1.f, e));
+        if (sub == 0) scales[v] = __float2half_rn(pow2f(e));
       }
     }
   }
