@@ -54,6 +54,8 @@ def parse():
     ap.add_argument("--per-shape", action="store_true", help="also time each shape alone")
     ap.add_argument("--crossover", action="store_true",
                     help="also time the GEMV (M = 1) and the tcgen05 GEMM at small M on two layer shapes")
+    ap.add_argument("--tc-rates", action="store_true",
+                    help="only measure tensor-core instruction rates (tcgen05 kind::f16, mma.sync f16 and s8)")
     return ap.parse_args()
 
 
@@ -829,8 +831,58 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_tc_rates(args):
+    """Sustained tensor-core rates on one GPU, for the int8 ("MMQ") question: tcgen05.mma
+    kind::f16 (the GEMM's instruction) against the warp-level mma.sync f16 and s8 instructions
+    (tcgen05.mma kind::i8 does not assemble for sm_103a).  Operands resident, zero-valued;
+    CUDA events around each launch."""
+    import ctypes
+
+    import torch
+
+    import __graft_entry__
+
+    lib = ctypes.CDLL(__graft_entry__._load_builder().build_microbench())
+    lib.jllm_microbench_tc_rate.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                            ctypes.c_void_p, ctypes.c_void_p]
+    lib.jllm_microbench_tc_rate.restype = ctypes.c_int
+    dev = torch.device("cuda", 0)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    stream = torch.cuda.Stream()
+    sink = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = {"sms": sms}
+    # (kind, name, CTAs, warps per CTA measured, ops per instruction, instructions per iteration per issuer)
+    cases = ((0, "tcgen05_kind_f16", sms, 1, 2 * 128 * 256 * 16, 4),
+             (1, "mma_sync_f16_m16n8k16", 2 * sms, 8, 2 * 16 * 8 * 16, 4),
+             (2, "mma_sync_s8_m16n8k32", 2 * sms, 8, 2 * 16 * 8 * 32, 4))
+    for kind, name, ctas, wpc, ops, per_iter in cases:
+        cyc = torch.zeros(ctas * wpc, dtype=torch.int64, device=dev)
+        best = None
+        for iters in (2000, 20000, 20000):
+            start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            start.record(stream)
+            rc = lib.jllm_microbench_tc_rate(kind, ctas, iters, cyc.data_ptr(), sink.data_ptr(), stream.cuda_stream)
+            end.record(stream)
+            end.synchronize()
+            if rc != 0:
+                raise RuntimeError(f"{name}: microbench returned {rc}")
+            t = start.elapsed_time(end) / 1e3
+            rate = ctas * wpc * iters * per_iter * ops / t / 1e12
+            best = max(best or 0.0, rate)
+        c = cyc.double()
+        out[name] = {"tops": round(best, 1), "cycles_per_instr_per_issuer": round(float(c.max()) / (20000 * per_iter), 2)}
+    out["tcgen05_kind_i8"] = "not available: ptxas (CUDA 13.0) rejects tcgen05.mma .kind::i8 for sm_103a"
+    peaks = load_peaks()
+    out["measured_cublas_bf16_tflops"] = peaks.get("bf16_tflops")
+    print(json.dumps({"tc_rates": out}), flush=True)
+
+
 def main():
     args = parse()
+    if args.tc_rates:
+        run_tc_rates(args)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:
