@@ -327,8 +327,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // ------------------------------------------------------------ MMA issuer --
       // Descriptors are a per-stage base plus 2 per K = 16 slice (32 bytes >> 4
       // in the start-address field, which cannot carry within shared memory),
-      // and the barriers of step k+1 are probed before step k's MMAs are issued
-      // so that the probe's latency overlaps the issue.
+      // and the barriers of step k+1 are probed (non-blocking test) before step
+      // k's MMAs are issued so that the probe's latency overlaps the issue.
       const uint32_t idesc = umma_idesc_f16(TILE_N, p.BN);
       const uint64_t adesc0 = umma_desc_sw128(sa), bdesc0 = umma_desc_sw128(sx);
       const uint32_t a_step = (uint32_t)(NMAT * A_STAGE_BYTES) >> 4, b_step = p.x_stage_bytes >> 4;
@@ -345,8 +345,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)racc.s * ACC_COLS;
-        bool x_ready = mbar_try_wait(b_xfull + 8 * rx.s, rx.ph);
-        bool a_ready = mbar_try_wait(b_afull + 8 * ra.s, ra.ph);
+        bool x_ready = mbar_test_wait(b_xfull + 8 * rx.s, rx.ph);
+        bool a_ready = mbar_test_wait(b_afull + 8 * ra.s, ra.ph);
         for (int k = it.k0; k < it.k1; ++k) {
           if ((!x_ready && !wait(b_xfull + 8 * rx.s, rx.ph)) || (!a_ready && !wait(b_afull + 8 * ra.s, ra.ph))) {
             ok = false;
@@ -358,8 +358,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           ra.next();
           rx.next();
           if (k + 1 < it.k1) {
-            x_ready = mbar_try_wait(b_xfull + 8 * rx.s, rx.ph);
-            a_ready = mbar_try_wait(b_afull + 8 * ra.s, ra.ph);
+            x_ready = mbar_test_wait(b_xfull + 8 * rx.s, rx.ph);
+            a_ready = mbar_test_wait(b_afull + 8 * ra.s, ra.ph);
           }
           const uint32_t acc0 = k > it.k0 ? 1u : 0u;
           umma_f16(d, ad, bd, idesc, acc0);
@@ -597,7 +597,57 @@ cudaError_t get_encoder(PFN_cuTensorMapEncodeTiled_v12000* out) {
   return g_encode ? cudaSuccess : cudaErrorNotSupported;
 }
 
+// Encoded tensor maps depend only on the device, the base address, the extents
+// and the box, so repeated calls on the same buffers reuse them: a small table
+// with least-recently-used replacement, shared by all threads under a mutex.
+struct MapKey {
+  int dev, kind;  // kind 0: X map, 1: W map
+  const void* ptr;
+  int64_t a, b;   // X: M, K; W: N, K
+  int box;        // X: tokens per tile; W: 0
+  bool operator==(const MapKey& o) const {
+    return dev == o.dev && kind == o.kind && ptr == o.ptr && a == o.a && b == o.b && box == o.box;
+  }
+};
+struct MapEntry {
+  MapKey key;
+  CUtensorMap map;
+  uint64_t stamp = 0;  // 0: empty
+};
+constexpr int kMapCache = 64;
+MapEntry g_map_cache[kMapCache];
+uint64_t g_map_clock = 0;
+std::mutex g_map_mu;
+
+bool map_lookup(const MapKey& k, CUtensorMap* out) {
+  std::lock_guard<std::mutex> lock(g_map_mu);
+  for (MapEntry& e : g_map_cache)
+    if (e.stamp && e.key == k) {
+      e.stamp = ++g_map_clock;
+      *out = e.map;
+      return true;
+    }
+  return false;
+}
+
+void map_insert(const MapKey& k, const CUtensorMap& m) {
+  std::lock_guard<std::mutex> lock(g_map_mu);
+  MapEntry* victim = &g_map_cache[0];
+  for (MapEntry& e : g_map_cache) {
+    if (e.stamp == 0) {
+      victim = &e;
+      break;
+    }
+    if (e.stamp < victim->stamp) victim = &e;
+  }
+  victim->key = k;
+  victim->map = m;
+  victim->stamp = ++g_map_clock;
+}
+
 cudaError_t make_x_map(const void* x, int64_t M, int64_t K, int BN, CUtensorMap* mx) {
+  const MapKey key{device_info().device, 0, x, M, K, BN};
+  if (map_lookup(key, mx)) return cudaSuccess;
   PFN_cuTensorMapEncodeTiled_v12000 enc;
   cudaError_t e = get_encoder(&enc);
   if (e != cudaSuccess) return e;
@@ -609,12 +659,15 @@ cudaError_t make_x_map(const void* x, int64_t M, int64_t K, int BN, CUtensorMap*
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
+  map_insert(key, *mx);
   return cudaSuccess;
 }
 
 // Byte view of a packed weight matrix: (144 bytes, super-block, row), one
 // super-block of 128 rows per load.
 cudaError_t make_w_map(const void* w, int64_t N, int64_t K, CUtensorMap* mw) {
+  const MapKey key{device_info().device, 1, w, N, K, 0};
+  if (map_lookup(key, mw)) return cudaSuccess;
   PFN_cuTensorMapEncodeTiled_v12000 enc;
   cudaError_t e = get_encoder(&enc);
   if (e != cudaSuccess) return e;
@@ -627,6 +680,7 @@ cudaError_t make_w_map(const void* w, int64_t N, int64_t K, CUtensorMap* mw) {
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
+  map_insert(key, *mw);
   return cudaSuccess;
 }
 

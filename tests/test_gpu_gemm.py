@@ -126,3 +126,27 @@ def test_gemm_long_prefill_shapes(q, name, K, N, M):
 
 def test_no_device_error_after_gemms(q):
     assert q.jllm_get_device_error() == q.JLLM_OK
+
+
+def test_tensor_map_cache_keys_on_address_and_shape(q):
+    """The GEMM reuses encoded tensor maps per (device, address, extents, box): the same buffer
+    reused for new contents, a new buffer at a recycled address, and the same address seen with
+    other extents must all compute the right product."""
+    import torch
+
+    K, M = 2560, 64
+    x1 = synthetic.activations(M, K, 1500)
+    big = synthetic.q4k_weights(384, K, 1501)
+    wd = dev(big)
+    for N in (384, 256, 130):  # one address, three row counts
+        ref, s = oracle.matmul(big[:N], x1, N, K)
+        y = q.jllm_q4k_gemm(wd[:N], dev(x1), N, K, out_dtype=torch.float32).cpu().numpy()
+        assert_within(y, ref, s, f"N={N}")
+    for seed in (1502, 1503):  # new contents in a buffer at (very likely) a recycled address
+        del wd
+        w = synthetic.q4k_weights(384, K, seed)
+        wd = dev(w)
+        xd = dev(synthetic.activations(M, K, seed + 10))
+        ref, s = oracle.matmul(w, xd.cpu().numpy(), 384, K)
+        y = q.jllm_q4k_gemm(wd, xd, 384, K, out_dtype=torch.float32).cpu().numpy()
+        assert_within(y, ref, s, f"seed={seed}")
