@@ -115,14 +115,25 @@ constexpr int SLOT_FLOATS = TILE_N * 256;           // fp32 partial of one tile 
 #endif
 constexpr uint64_t WAIT_LIMIT_NS = JLLM_WAIT_LIMIT_NS;  // 2 s (a test build shortens it)
 
-template <bool SWIGLU>
+// ATMEM: the dequantised weight tile (the MMA's A operand) is written to
+// tensor memory with tcgen05.st instead of shared memory, so the tensor core
+// reads only X from shared memory.  Tensor memory then holds two accumulators
+// of at most ACC_COLS_ATMEM columns and SA A stages of 32 columns (128 rows x
+// 64 fp16, two per 32-bit column).
+constexpr uint32_t ACC_COLS_ATMEM = 128;
+constexpr uint32_t A_TMEM_COL0 = 2 * ACC_COLS_ATMEM;  // first column of the A ring
+constexpr uint32_t A_TMEM_STAGE_COLS = KSTEP / 2;     // 32
+
+template <bool SWIGLU, bool ATMEM = false>
 struct Cfg {
-  static constexpr int NMAT = SWIGLU ? 2 : 1;  // weight matrices per tile
-  static constexpr int SX = 3;                 // X ring
-  static constexpr int SA = SWIGLU ? 3 : 4;    // dequantised-A ring
-  static constexpr int SW = SWIGLU ? 2 : 3;    // raw-W ring
-  static constexpr int BN_MAX = SWIGLU ? 128 : 256;
+  static constexpr int NMAT = SWIGLU ? 2 : 1;            // weight matrices per tile
+  static constexpr int SX = ATMEM ? 6 : 3;               // X ring
+  static constexpr int SA = SWIGLU ? 3 : (ATMEM ? 8 : 4); // dequantised-A ring
+  static constexpr int SW = SWIGLU ? 2 : 3;              // raw-W ring
+  static constexpr int BN_MAX = SWIGLU ? 128 : (ATMEM ? (int)ACC_COLS_ATMEM : 256);
+  static constexpr uint32_t ACC = ATMEM ? ACC_COLS_ATMEM : ACC_COLS;  // TMEM columns per accumulator
   static constexpr int NBARS = 2 * (SX + SA + SW) + 2 + 2 + 1;
+  static_assert(!ATMEM || (!SWIGLU && A_TMEM_COL0 + SA * A_TMEM_STAGE_COLS <= TMEM_COLS), "tensor memory budget");
 };
 
 // Up to kMaxGemmBatch weight matrices that share X (and so K) run in one
@@ -212,11 +223,33 @@ struct UnitIter {
   }
 };
 
-template <bool SWIGLU>
+// acc += A * B^T with A (128 x 16 fp16) in tensor memory at column a_tmem.
+__device__ __forceinline__ void umma_f16_ta(uint32_t tmem_d, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(tmem_d),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// 32 lanes x 16 columns of 32-bit words: thread i of the warp writes lane
+// (base lane + i), columns col..col+15.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0],"
+      " {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+template <bool SWIGLU, bool ATMEM>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     q4k_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ WMaps tmW,
                        const __grid_constant__ GemmParams p) {
-  using C = Cfg<SWIGLU>;
+  using C = Cfg<SWIGLU, ATMEM>;
   constexpr int NMAT = C::NMAT, SX = C::SX, SA = C::SA, SW = C::SW;
   extern __shared__ uint8_t gemm_smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(gemm_smem_raw) + 1023) & ~uintptr_t(1023));
@@ -344,7 +377,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t d = tmem + (uint32_t)racc.s * ACC_COLS;
+        const uint32_t d = tmem + (uint32_t)racc.s * C::ACC;
         bool x_ready = mbar_test_wait(b_xfull + 8 * rx.s, rx.ph);
         bool a_ready = mbar_test_wait(b_afull + 8 * ra.s, ra.ph);
         for (int k = it.k0; k < it.k1; ++k) {
@@ -362,12 +395,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             a_ready = mbar_test_wait(b_afull + 8 * ra.s, ra.ph);
           }
           const uint32_t acc0 = k > it.k0 ? 1u : 0u;
-          umma_f16(d, ad, bd, idesc, acc0);
-          if (SWIGLU) umma_f16(d + 128, ad + A2, bd, idesc, acc0);
+          if (ATMEM) {
+            const uint32_t at = tmem + A_TMEM_COL0 + sa_now * A_TMEM_STAGE_COLS;
 #pragma unroll
-          for (int kk = 1; kk < KSTEP / 16; ++kk) {
-            umma_f16(d, ad + 2 * kk, bd + 2 * kk, idesc, 1u);
-            if (SWIGLU) umma_f16(d + 128, ad + A2 + 2 * kk, bd + 2 * kk, idesc, 1u);
+            for (int kk = 0; kk < KSTEP / 16; ++kk) umma_f16_ta(d, at + 8 * kk, bd + 2 * kk, idesc, kk ? 1u : acc0);
+          } else {
+            umma_f16(d, ad, bd, idesc, acc0);
+            if (SWIGLU) umma_f16(d + 128, ad + A2, bd, idesc, acc0);
+#pragma unroll
+            for (int kk = 1; kk < KSTEP / 16; ++kk) {
+              umma_f16(d, ad + 2 * kk, bd + 2 * kk, idesc, 1u);
+              if (SWIGLU) umma_f16(d + 128, ad + A2 + 2 * kk, bd + 2 * kk, idesc, 1u);
+            }
           }
           umma_commit(b_aempty + 8 * sa_now);
           umma_commit(b_xempty + 8 * sx_now);
@@ -420,24 +459,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const unsigned short d16 = (unsigned short)(hd.x & 0xffffu);
           const float nt = -__fmul_rn(half_hi_to_float(hd.x), (float)m);
           const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-          uint8_t* arow = smem + p.off_a + (size_t)(ra.s * NMAT + mat) * A_STAGE_BYTES + (size_t)r * 128;
+          uint32_t pk[16];  // fp16 pairs (k, k+1) for k = 32*hs + 2*i of the step
 #pragma unroll
-          for (int jj = 0; jj < 4; ++jj) {
-            // output chunk j8 = 4*hs + jj holds k = 8*j8..8*j8+7: code bytes 8*jj..8*jj+7
-            uint32_t pk[4];
+          for (int i = 0; i < 8; ++i) {
+            uint32_t wp;
+            asm("prmt.b32 %0, %1, 0, 0x3120;" : "=r"(wp) : "r"(qw[i]));  // bytes b0 b2 b1 b3
+            pk[2 * i] = dq_pair(lop3_and_or(wp, mask, 0x64006400u), scv_u, offv_u, d16, nt);           // k, k+1
+            pk[2 * i + 1] = dq_pair(lop3_and_or(wp >> 8, mask, 0x64006400u), scv_u, offv_u, d16, nt);  // k+2, k+3
+          }
+          if (ATMEM) {
+            // lane r of the warp's TMEM quarter, 16 columns of the step's 32 (two fp16 per column)
+            tmem_st16(tmem + ((uint32_t)(32 * q) << 16) + A_TMEM_COL0 + ra.s * A_TMEM_STAGE_COLS + 16 * hs, pk);
+          } else {
+            uint8_t* arow = smem + p.off_a + (size_t)(ra.s * NMAT + mat) * A_STAGE_BYTES + (size_t)r * 128;
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const uint32_t w = qw[2 * jj + e];
-              uint32_t wp;
-              asm("prmt.b32 %0, %1, 0, 0x3120;" : "=r"(wp) : "r"(w));  // bytes b0 b2 b1 b3
-              pk[2 * e] = dq_pair(lop3_and_or(wp, mask, 0x64006400u), scv_u, offv_u, d16, nt);       // k, k+1
-              pk[2 * e + 1] = dq_pair(lop3_and_or(wp >> 8, mask, 0x64006400u), scv_u, offv_u, d16, nt);  // k+2, k+3
+            for (int jj = 0; jj < 4; ++jj) {  // output chunk j8 = 4*hs + jj holds k = 8*j8..8*j8+7
+              const int j8 = 4 * hs + jj;
+              *reinterpret_cast<uint4*>(arow + ((j8 ^ (r & 7)) << 4)) =
+                  make_uint4(pk[4 * jj], pk[4 * jj + 1], pk[4 * jj + 2], pk[4 * jj + 3]);
             }
-            const int j8 = 4 * hs + jj;
-            *reinterpret_cast<uint4*>(arow + ((j8 ^ (r & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
           }
         }
-        fence_proxy_async_smem();
+        if (ATMEM) tc_fence_before();
+        else fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(b_afull + 8 * ra.s);
         ra.next();
@@ -461,7 +505,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ok = mbar_wait_warp_sleepy(b_accfull + 8 * racc.s, racc.ph, abort_flag, WAIT_LIMIT_NS);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)racc.s * ACC_COLS;
+      const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)racc.s * C::ACC;
       const TileLoc loc = locate(p, it.tile);
       const int n = loc.n0 + r, m0 = loc.m0;
       const bool writer = it.k0 > 0;                  // later part of a cut tile
@@ -691,9 +735,11 @@ cudaError_t make_w_map(const void* w, int64_t N, int64_t K, CUtensorMap* mw) {
 // They are fixed in the shipped library.  A build with -DJLLM_TUNING reads
 // overrides once from the environment (JLLM_GEMM_BN, JLLM_GEMM_SPLIT), for
 // measurements only.
+//   atmem  1: the A operand in tensor memory (single-GEMM and batched launches)
 struct GemmKnobs {
   int bn = 0;
   int split = 1;
+  int atmem = 1;
 };
 const GemmKnobs& gemm_knobs() {
   static GemmKnobs k = [] {
@@ -701,16 +747,17 @@ const GemmKnobs& gemm_knobs() {
 #ifdef JLLM_TUNING
     if (const char* e = getenv("JLLM_GEMM_BN")) v.bn = atoi(e);
     if (const char* e = getenv("JLLM_GEMM_SPLIT")) v.split = atoi(e);
+    if (const char* e = getenv("JLLM_GEMM_ATMEM")) v.atmem = atoi(e);
 #endif
     return v;
   }();
   return k;
 }
 
-template <bool SWIGLU>
+template <bool SWIGLU, bool ATMEM>
 cudaError_t launch_tc(const CUtensorMap& mx, const WMaps& mw, const GemmParams& p, int grid, bool cooperative,
                       size_t smem, cudaStream_t s) {
-  auto kern = q4k_gemm_tc_kernel<SWIGLU>;
+  auto kern = q4k_gemm_tc_kernel<SWIGLU, ATMEM>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -817,6 +864,10 @@ cudaError_t launch_tc_common(const void* const* w, const void* w1, const int64_t
   for (int b = 0; b < count; ++b) n_tiles += Ns[b] > 0 ? (Ns[b] + TILE_N - 1) / TILE_N : 0;
   if (kn.bn == 0 && M > bn_cap / 2 && M <= bn_cap && 2 * n_tiles <= dev.sm_count)
     BN = (int)(((M + 1) / 2 + 15) / 16 * 16);
+  // Tiles of at most 128 tokens keep the dequantised A operand in tensor memory
+  // (9-12 % faster than in shared memory at the same tile width, measured at 128
+  // and 192 tokens); wider tiles need all 512 columns for two accumulators.
+  const bool atmem = !swiglu && kn.atmem != 0 && BN <= 128;
 
   GemmParams p = {};
   p.M = (int)M;
@@ -859,15 +910,16 @@ cudaError_t launch_tc_common(const void* const* w, const void* w1, const int64_t
     p.grains = tiles;
   }
 
-  // Shared memory: X ring, dequantised-A ring, raw-W ring, barriers.
-  const int SX = swiglu ? Cfg<true>::SX : Cfg<false>::SX;
-  const int SA = swiglu ? Cfg<true>::SA : Cfg<false>::SA;
-  const int SW = swiglu ? Cfg<true>::SW : Cfg<false>::SW;
-  const int nbars = swiglu ? Cfg<true>::NBARS : Cfg<false>::NBARS;
+  // Shared memory: X ring, dequantised-A ring (not with A in tensor memory),
+  // raw-W ring, barriers.
+  const int SX = swiglu ? Cfg<true>::SX : (atmem ? Cfg<false, true>::SX : Cfg<false>::SX);
+  const int SA = swiglu ? Cfg<true>::SA : (atmem ? Cfg<false, true>::SA : Cfg<false>::SA);
+  const int SW = swiglu ? Cfg<true>::SW : (atmem ? Cfg<false, true>::SW : Cfg<false>::SW);
+  const int nbars = swiglu ? Cfg<true>::NBARS : (atmem ? Cfg<false, true>::NBARS : Cfg<false>::NBARS);
   p.x_stage_bytes = (uint32_t)BN * KSTEP * 2;
   p.off_x = 0;
   p.off_a = (uint32_t)SX * p.x_stage_bytes;
-  p.off_w = p.off_a + (uint32_t)(SA * nmat * A_STAGE_BYTES);
+  p.off_w = p.off_a + (atmem ? 0u : (uint32_t)(SA * nmat * A_STAGE_BYTES));
   p.off_bar = p.off_w + (uint32_t)(SW * nmat * W_STAGE_BYTES);
   const size_t smem = 1024 + p.off_bar + 8 * nbars + 16;
   if (smem > dev.smem_optin) return cudaErrorInvalidValue;
@@ -879,7 +931,9 @@ cudaError_t launch_tc_common(const void* const* w, const void* w1, const int64_t
   for (int b = 0; b < count && e == cudaSuccess; ++b) e = make_w_map(w[b], Ns[b], K, &mw.w[b]);
   if (e == cudaSuccess && swiglu) e = make_w_map(w1, Ns[0], K, &mw.w[1]);
   if (e != cudaSuccess) return e;
-  return swiglu ? launch_tc<true>(mx, mw, p, grid, split, smem, s) : launch_tc<false>(mx, mw, p, grid, split, smem, s);
+  if (swiglu) return launch_tc<true, false>(mx, mw, p, grid, split, smem, s);
+  return atmem ? launch_tc<false, true>(mx, mw, p, grid, split, smem, s)
+               : launch_tc<false, false>(mx, mw, p, grid, split, smem, s);
 }
 
 }  // namespace
