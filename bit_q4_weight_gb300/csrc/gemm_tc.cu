@@ -306,32 +306,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   };
 
   if (warp == 0) {
+    // ----------------------------------------------------------- TMA producers --
+    // Lane 0 streams the X tiles, lane 1 the raw weight blocks: each runs ahead
+    // as far as its own ring allows (W up to SW blocks = 4*SW K steps ahead of
+    // the dequantisers, X up to SX steps ahead of the MMA), so a W copy is not
+    // held back by the X ring.
     if (lane == 0) {
-      // ---------------------------------------------------------- TMA producer --
       tma_prefetch_desc(&tmX);
-      for (int i = 0; i < (SWIGLU ? 2 : p.count); ++i) tma_prefetch_desc(&tmW.w[i]);
       Ring<SX> rx;
-      Ring<SW> rw;
-      long long nx = 0, nw = 0;
+      long long nx = 0;
       bool ok = true;
       UnitIter it{u_begin, u_end, p.KS};
       while (ok && it.next()) {
-        const TileLoc loc = locate(p, it.tile);
-        const int n0 = loc.n0, m0 = loc.m0;
-        const CUtensorMap* mw = &tmW.w[loc.b];
+        const int m0 = locate(p, it.tile).m0;
         for (int k = it.k0; k < it.k1; ++k) {
-          if (k == it.k0 || (k & 3) == 0) {
-            if (!wait(b_wempty + 8 * rw.s, rw.ph ^ 1u)) {
-              ok = false;
-              break;
-            }
-            const uint32_t bar = b_wfull + 8 * rw.s;
-            mbar_arrive_expect_tx(bar, W_STAGE_BYTES * NMAT);
-            tma_load_3d(sw + (uint32_t)(rw.s * NMAT) * W_STAGE_BYTES, mw, bar, 0, k >> 2, n0);
-            if (SWIGLU) tma_load_3d(sw + (uint32_t)(rw.s * NMAT + 1) * W_STAGE_BYTES, &tmW.w[1], bar, 0, k >> 2, n0);
-            rw.next();
-            ++nw;
-          }
           if (!wait(b_xempty + 8 * rx.s, rx.ph ^ 1u)) {
             ok = false;
             break;
@@ -352,6 +340,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // Every copy this thread issued must have landed before the CTA exits.
       for (long long i = nx > SX ? nx - SX : 0; i < nx; ++i)
         mbar_wait_bounded(b_xfull + 8 * (int)(i % SX), (uint32_t)((i / SX) & 1), nullptr, WAIT_LIMIT_NS);
+    } else if (lane == 1) {
+      for (int i = 0; i < (SWIGLU ? 2 : p.count); ++i) tma_prefetch_desc(&tmW.w[i]);
+      Ring<SW> rw;
+      long long nw = 0;
+      bool ok = true;
+      UnitIter it{u_begin, u_end, p.KS};
+      while (ok && it.next()) {
+        const TileLoc loc = locate(p, it.tile);
+        const CUtensorMap* mw = &tmW.w[loc.b];
+        for (int k = it.k0; k < it.k1; ++k) {
+          if (k == it.k0 || (k & 3) == 0) {
+            if (!wait(b_wempty + 8 * rw.s, rw.ph ^ 1u)) {
+              ok = false;
+              break;
+            }
+            const uint32_t bar = b_wfull + 8 * rw.s;
+            mbar_arrive_expect_tx(bar, W_STAGE_BYTES * NMAT);
+            tma_load_3d(sw + (uint32_t)(rw.s * NMAT) * W_STAGE_BYTES, mw, bar, 0, k >> 2, loc.n0);
+            if (SWIGLU) tma_load_3d(sw + (uint32_t)(rw.s * NMAT + 1) * W_STAGE_BYTES, &tmW.w[1], bar, 0, k >> 2, loc.n0);
+            rw.next();
+            ++nw;
+          }
+        }
+      }
+      if (!ok) fail();
       for (long long i = nw > SW ? nw - SW : 0; i < nw; ++i)
         mbar_wait_bounded(b_wfull + 8 * (int)(i % SW), (uint32_t)((i / SW) & 1), nullptr, WAIT_LIMIT_NS);
     }
