@@ -45,8 +45,9 @@
  * A launch failure returns JLLM_ERR_CUDA.  Kernel-side waits are bounded: a
  * wait that runs out sets a device error word that jllm_get_device_error()
  * reads.  No call throws or prints.  State kept: cached device properties,
- * the driver's tensor-map encoder, and the static workspace of
- * jllm_q4k_gemm_noalloc.  Environment variables read (once per process):
+ * the driver's tensor-map encoder, a table of the 64 most recently used
+ * encoded tensor maps (keyed by device, address, extents and tile; guarded by
+ * a mutex), and the static workspace of jllm_q4k_gemm_noalloc.  Environment variables read (once per process):
  * JLLM_PDL and JLLM_GEMV_MAX_M, described below; no other setting changes
  * launch shapes or summation order.
  * The GEMV and GEMM kernels are launched with programmatic dependent launch:
@@ -173,9 +174,10 @@ jllm_status jllm_q4k_gemv_rmsnorm_batch(const void* const* w_q4k, float* const* 
  *   x     : [K] fp16; gamma: [K] fp32 or NULL, eps in [0, 1]
  *   q_gamma, k_gamma: [128] fp32 or NULL; head_eps in [0, 1]
  *   pos   : token position (any 32-bit value); rope_base > 0 (Qwen3: 1e6)
- * Head size 128 only.  The angle is formed in fp64 and its cosine and sine
- * rounded to fp32; each q/k value stays within the matmul bound propagated
- * through the norm and the rotation.  The 8 CTAs that compute one head form
+ * Head size 128 only.  base^(-2j/128) is formed on the host in fp64, the angle
+ * and its reduction modulo 2 pi in fp64, the cosine and sine in fp32; each q/k
+ * value stays within the matmul bound propagated through the norm and the
+ * rotation.  The 8 CTAs that compute one head form
  * a thread-block cluster and reduce the head's sum of squares through
  * distributed shared memory.  gamma, q_gamma and k_gamma, like the weights,
  * must not be written by the kernel enqueued just before (PDL paragraph).
