@@ -77,13 +77,34 @@ __global__ void __launch_bounds__(KV_THREADS, 5) kv_encode_kernel(const uint4* _
 #pragma unroll
       for (int o = L / 2; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
       const int e = kv_exponent(__half2float(__ushort_as_half((unsigned short)m)));
-      const float inv = pow2f(-e);
       if (v < n_vec) {
-        const __half2* h = reinterpret_cast<const __half2*>(&u[j]);
-        float2 f0 = __half22float2(h[0]), f1 = __half22float2(h[1]), f2 = __half22float2(h[2]), f3 = __half22float2(h[3]);
         uint2 out;
-        out.x = pack4_i8(code_of(f0.x, inv), code_of(f0.y, inv), code_of(f1.x, inv), code_of(f1.y, inv));
-        out.y = pack4_i8(code_of(f2.x, inv), code_of(f2.y, inv), code_of(f3.x, inv), code_of(f3.y, inv));
+        if (e >= -14) {
+          // fp16 pairs: fma(v, 2^-e, 1536) is v / 2^e + 1536 rounded once to the fp16 grid of
+          // [1024, 2048), whose step is 1: round half to even of v / 2^e, plus 1536.  The
+          // bits are then 0x6600 + q, so the low byte is q as a two's-complement int8.
+          // |v / 2^e| <= 127 except when e is clamped at 9 (max |v| > 65280): clamp there.
+          const uint32_t inv = (uint32_t)(15 - e) << 10;  // fp16 2^-e
+          const uint32_t inv2 = inv | (inv << 16);
+          uint32_t r[4];
+          const uint32_t w[4] = {u[j].x, u[j].y, u[j].z, u[j].w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r[i]) : "r"(w[i]), "r"(inv2), "r"(0x66006600u));
+            if (e == 9) {  // 1536 -/+ 127 = 0x6581 / 0x667F
+              asm("max.f16x2 %0, %0, %1;" : "+r"(r[i]) : "r"(0x65816581u));
+              asm("min.f16x2 %0, %0, %1;" : "+r"(r[i]) : "r"(0x667F667Fu));
+            }
+          }
+          out.x = __byte_perm(r[0], r[1], 0x6420);  // low bytes of the four halves
+          out.y = __byte_perm(r[2], r[3], 0x6420);
+        } else {
+          const float inv = pow2f(-e);
+          const __half2* h = reinterpret_cast<const __half2*>(&u[j]);
+          float2 f0 = __half22float2(h[0]), f1 = __half22float2(h[1]), f2 = __half22float2(h[2]), f3 = __half22float2(h[3]);
+          out.x = pack4_i8(code_of(f0.x, inv), code_of(f0.y, inv), code_of(f1.x, inv), code_of(f1.y, inv));
+          out.y = pack4_i8(code_of(f2.x, inv), code_of(f2.y, inv), code_of(f3.x, inv), code_of(f3.y, inv));
+        }
         codes[v * L + sub] = out;
         if (sub == 0) scales[v] = __float2half_rn(pow2f(e));
       }
