@@ -288,6 +288,19 @@ def run_ours(args):
     value = total_bytes * world / t_max / 1e9
     del g
 
+    # the same sweep as ONE call: jllm_q4k_gemv_chain (one persistent launch for the 144 steps)
+    chain = q.GemvChain(plan)
+    with torch.cuda.stream(stream):
+        chain(stream)
+    torch.cuda.synchronize()
+    gc = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gc, stream=stream):
+        chain(stream)
+    torch.cuda.synchronize()
+    sync_ranks()
+    tc = tmax(time_graph(torch, gc, stream, args.steps, args.warmup))
+    del gc
+
     # the same weights, seven single-matrix launches per layer
     plan7 = decode_plan(W, XG, Y, meta, batched=False)
     g7 = capture(plan7)
@@ -407,6 +420,26 @@ def run_ours(args):
                     "ms_per_step": round(t_eager * 1e3, 4),
                     "how": "the same copies, the 144 C-ABI calls issued eagerly from Python (ctypes) every step"}
 
+    # the same end to end through ONE eager C-ABI call per step: jllm_q4k_gemv_chain
+    chain_e = q.GemvChain(decode_plan(W, XGv, Yv, meta, batched=True))
+
+    def e2e_chain_step():
+        with torch.cuda.stream(stream):
+            x_dev_all.copy_(xs_host, non_blocking=True)
+            chain_e(stream)
+            ys_host.copy_(y_dev_all, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(args.warmup):
+        e2e_chain_step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        e2e_chain_step()
+    t_ce = tmax((time.perf_counter() - t0) / args.steps)
+    e2e["chain_eager"] = {"value": round(total_bytes * world / t_ce / 1e9, 2), "unit": "GB/s",
+                          "ms_per_step": round(t_ce * 1e3, 4),
+                          "how": "the same copies around one eager jllm_q4k_gemv_chain call (all 144 steps)"}
+
     peaks = {}
     pk_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(pk_path):
@@ -474,6 +507,9 @@ def run_ours(args):
                          "kernel": "q4k_gemv_kernel", "avg_launch_us": round(t_step / n_launch * 1e6, 3),
                          "frac_of_nominal_7900": round(total_bytes / t_step / 1e9 / 7900.0, 4)},
             "e2e": e2e,
+            "decode_chain": {"value": round(total_bytes * world / tc / 1e9, 2), "unit": "GB/s",
+                             "ms_per_step": round(tc * 1e3, 4), "launches_per_step": 1,
+                             "workload": "the batched decode sweep (144 steps) as one jllm_q4k_gemv_chain call"},
             "decode_7call": {"value": round(total_bytes * world / t7 / 1e9, 2), "unit": "GB/s",
                              "ms_per_step": round(t7 * 1e3, 4), "launches_per_step": len(plan7)},
             "decode_rmsnorm_fused": {"value": round(total_bytes * world / tn / 1e9, 2), "unit": "GB/s",

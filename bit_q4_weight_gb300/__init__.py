@@ -42,6 +42,8 @@ EXPORTS = (
     "jllm_q4k_gemv_batch",
     "jllm_q4k_gemv_rmsnorm_batch",
     "jllm_q4k_gemv_qkv_rope",
+    "jllm_q4k_gemv_chain",
+    "jllm_q4k_gemv_chain_sync_bytes",
     "jllm_q4k_gemm",
     "jllm_q4k_gemm_noalloc",
     "jllm_q4k_gemm_batch",
@@ -84,6 +86,22 @@ lib.jllm_q4k_gemv_rmsnorm_batch.restype = _ST
 lib.jllm_q4k_gemv_qkv_rope.argtypes = [_P, _P, _I64, _I64, _P, _I64, _P, ctypes.c_float, _P, _P, ctypes.c_float,
                                        _I64, ctypes.c_float, _P]
 lib.jllm_q4k_gemv_qkv_rope.restype = _ST
+CHAIN_MAX_STEPS = 256
+CHAIN_MAX_MATS = 4
+CHAIN_MAX_K = 12288
+
+
+class GemvStep(ctypes.Structure):
+    """jllm_gemv_step of the header."""
+    _fields_ = [("count", ctypes.c_int32), ("y_f16", ctypes.c_int32), ("K", ctypes.c_int64),
+                ("x", ctypes.c_void_p), ("w_q4k", ctypes.c_void_p * CHAIN_MAX_MATS),
+                ("y", ctypes.c_void_p * CHAIN_MAX_MATS), ("N", ctypes.c_int64 * CHAIN_MAX_MATS)]
+
+
+lib.jllm_q4k_gemv_chain.argtypes = [ctypes.POINTER(GemvStep), ctypes.c_int, _P, _P]
+lib.jllm_q4k_gemv_chain.restype = _ST
+lib.jllm_q4k_gemv_chain_sync_bytes.argtypes = [ctypes.c_int]
+lib.jllm_q4k_gemv_chain_sync_bytes.restype = _SZ
 lib.jllm_q4k_gemm.argtypes = [_P, _P, _P, ctypes.c_int, _I64, _I64, _I64, _P, _SZ, _P]
 lib.jllm_q4k_gemm.restype = _ST
 lib.jllm_q4k_gemm_noalloc.argtypes = [_P, _P, _P, ctypes.c_int, _I64, _I64, _I64, _P]
@@ -304,6 +322,83 @@ def jllm_q4k_gemv_qkv_rope(w_qkv, x, n_q_heads: int, n_kv_heads: int, K: int, po
                                       ptr(q_gamma), ptr(k_gamma), float(head_eps), int(pos), float(rope_base),
                                       _stream_ptr(stream)), "jllm_q4k_gemv_qkv_rope")
     return outs
+
+
+def jllm_q4k_gemv_chain_sync_bytes(n_steps: int) -> int:
+    return int(lib.jllm_q4k_gemv_chain_sync_bytes(int(n_steps)))
+
+
+class GemvChain:
+    """A jllm_q4k_gemv_chain call prepared once: `steps` is a sequence of
+    (ws_q4k, x, outs, Ns, K) -- the matrices of a step (1..4 uint8 [N_i, K/256*144]
+    tensors), its fp16 [K] x, its outputs (fp32 or fp16 [N_i], all one dtype) and
+    row counts.  The descriptors are packed here, with a zeroed sync buffer owned
+    by the object; calling it enqueues the whole chain (one launch).  The tensors
+    must stay alive while the object is used."""
+
+    def __init__(self, steps, device=None, sync=True):
+        torch = _torch()
+        steps = list(steps)
+        n = len(steps)
+        if not 1 <= n <= CHAIN_MAX_STEPS:
+            raise ValueError(f"a chain has 1..{CHAIN_MAX_STEPS} steps, got {n}")
+        self._arr = (GemvStep * n)()
+        self._keep = []
+        dev = None
+        for i, (ws_q4k, x, outs, Ns, K) in enumerate(steps):
+            cnt = len(ws_q4k)
+            if not 1 <= cnt <= CHAIN_MAX_MATS or len(outs) != cnt or len(Ns) != cnt:
+                raise ValueError(f"step {i}: 1..{CHAIN_MAX_MATS} matrices, as many outputs and row counts")
+            _need(x, torch.float16, (K,), f"steps[{i}].x")
+            f16 = outs[0].dtype == torch.float16
+            st = self._arr[i]
+            st.count, st.y_f16, st.K, st.x = cnt, int(f16), int(K), x.data_ptr()
+            for j in range(cnt):
+                _need(ws_q4k[j], torch.uint8, _w_shape(Ns[j], K), f"steps[{i}].w[{j}]")
+                _need(outs[j], torch.float16 if f16 else torch.float32, (Ns[j],), f"steps[{i}].y[{j}]")
+                st.w_q4k[j], st.y[j], st.N[j] = ws_q4k[j].data_ptr(), outs[j].data_ptr(), int(Ns[j])
+            dev = x.device
+        self.n_steps = n
+        self.sync = _chain_sync(n, device or dev, False) if sync else None
+
+    def __call__(self, stream=None):
+        _check(lib.jllm_q4k_gemv_chain(self._arr, self.n_steps, self.sync.data_ptr(), _stream_ptr(stream)),
+               "jllm_q4k_gemv_chain")
+
+
+# Zeroed sync buffers of one-shot chains, per (device, stream, steps): a chain
+# that completes leaves its buffer zeroed, and calls on one stream are ordered.
+_SYNC_CACHE = {}
+
+
+def _chain_sync(n, device, stream):
+    """A zeroed sync buffer for n steps: private (stream None) or shared per stream."""
+    torch = _torch()
+    device = torch.device(device)
+    idx = device.index if device.index is not None else torch.cuda.current_device()
+    key = (idx, _stream_ptr(stream), n) if stream is not False else None
+    buf = _SYNC_CACHE.get(key) if key else None
+    if buf is None:
+        buf = torch.zeros(jllm_q4k_gemv_chain_sync_bytes(n), dtype=torch.uint8, device=device)
+        torch.cuda.synchronize(device)  # zero before any stream uses it
+        if key:
+            _SYNC_CACHE[key] = buf
+    return buf
+
+
+def jllm_q4k_gemv_chain(steps, stream=None):
+    """One-shot jllm_q4k_gemv_chain over steps of (ws_q4k, x, outs, Ns, K) (see GemvChain);
+    outs given as None are allocated (fp32).  Returns the outputs, one list per step."""
+    torch = _torch()
+    filled = []
+    for ws_q4k, x, outs, Ns, K in steps:
+        if outs is None:
+            outs = [torch.empty(int(n), dtype=torch.float32, device=x.device) for n in Ns]
+        filled.append((ws_q4k, x, outs, Ns, K))
+    ch = GemvChain(filled, sync=False)
+    ch.sync = _chain_sync(ch.n_steps, filled[0][1].device, stream)
+    ch(stream)
+    return [o for (_, _, o, _, _) in filled]
 
 
 def jllm_q4k_gemm(w, x, N: int, K: int, out_dtype=None, out=None, ws=None, stream=None):

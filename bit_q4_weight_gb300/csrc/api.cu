@@ -186,6 +186,35 @@ jllm_status jllm_q4k_gemv_rmsnorm_batch(const void* const* w_q4k, float* const* 
                                                    eps, K, (cudaStream_t)stream));
 }
 
+jllm_status jllm_q4k_gemv_chain(const jllm_gemv_step* steps, int n_steps, uint32_t* sync, jllm_stream_t stream) {
+  if (!steps || !sync) return JLLM_ERR_INVALID_ARG;
+  if (n_steps < 1 || n_steps > JLLM_CHAIN_MAX_STEPS) return JLLM_ERR_INVALID_ARG;
+  if (((uintptr_t)sync & 3u) != 0) return JLLM_ERR_MISALIGNED;
+  for (int s = 0; s < n_steps; ++s) {
+    const jllm_gemv_step& d = steps[s];
+    if (!d.x || d.count < 1 || d.count > JLLM_CHAIN_MAX_MATS || (d.y_f16 != 0 && d.y_f16 != 1))
+      return JLLM_ERR_INVALID_ARG;
+    if (d.K <= 0 || d.K % 256 || d.K > JLLM_CHAIN_MAX_K) return JLLM_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(d.x)) return JLLM_ERR_MISALIGNED;
+    int64_t total = 0;
+    for (int i = 0; i < d.count; ++i) {
+      if (d.N[i] < 0) return JLLM_ERR_INVALID_ARG;
+      if (d.N[i] == 0) continue;
+      if (!d.w_q4k[i] || !d.y[i]) return JLLM_ERR_INVALID_ARG;
+      if (!aligned16(d.w_q4k[i]) || !aligned16(d.y[i])) return JLLM_ERR_MISALIGNED;
+      total += d.N[i];
+    }
+    if (total > kMaxRows) return JLLM_ERR_UNSUPPORTED_SHAPE;
+  }
+  jllm_status st = check_device();
+  if (st != JLLM_OK) return st;
+  return from_cuda(jllm::launch_gemv_chain(steps, n_steps, sync, (cudaStream_t)stream));
+}
+
+size_t jllm_q4k_gemv_chain_sync_bytes(int n_steps) {
+  return (n_steps < 1 || n_steps > JLLM_CHAIN_MAX_STEPS) ? 0 : sizeof(uint32_t) * (size_t)(n_steps + 1);
+}
+
 jllm_status jllm_q4k_gemv_qkv_rope(const void* const* w_q4k, float* const* y, int64_t n_q_heads,
                                    int64_t n_kv_heads, const void* x, int64_t K, const float* gamma, float eps,
                                    const float* q_gamma, const float* k_gamma, float head_eps, int64_t pos,
@@ -318,14 +347,15 @@ jllm_status jllm_kv_decode_i8(const int8_t* codes, const void* scales, void* kv,
 }
 
 jllm_status jllm_get_device_error(jllm_stream_t stream) {
-  uint32_t a = 0, b = 0;
+  uint32_t a = 0, b = 0, c = 0;
   cudaError_t e = jllm::read_clear_gemm_error(&a, (cudaStream_t)stream);
   if (e == cudaSuccess) e = jllm::read_clear_gemv_error(&b);
+  if (e == cudaSuccess) e = jllm::read_clear_chain_error(&c);
   // A tcgen05 kernel that gave up may have left stream-K flags set in the
   // library's static workspace: clear them before anyone calls again.
   if (e == cudaSuccess && a) e = jllm::gemm_static_workspace_reset((cudaStream_t)stream);
   if (e != cudaSuccess) return JLLM_ERR_CUDA;
-  return (a | b) ? JLLM_ERR_DEVICE_TIMEOUT : JLLM_OK;
+  return (a | b | c) ? JLLM_ERR_DEVICE_TIMEOUT : JLLM_OK;
 }
 
 #ifdef JLLM_FAULT_INJECTION
@@ -337,6 +367,10 @@ jllm_status jllm_test_fault_injection(int gemm_skip_x, int gemv_skip_w) {
   if (e == cudaSuccess) e = jllm::fault_injection_set_gemv(gemv_skip_w);
   return from_cuda(e);
 }
+
+// Test builds only: skip != 0 makes the producer of CTA 0 of the next GEMV
+// chains skip its first weight copy; 0 clears it.
+jllm_status jllm_test_fault_injection_chain(int skip) { return from_cuda(jllm::fault_injection_set_chain(skip)); }
 #endif
 
 }  // extern "C"

@@ -5,6 +5,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "jllm_q4k.h"
+
 namespace jllm {
 
 struct DevInfo {
@@ -50,6 +52,16 @@ cudaError_t launch_gemv_qkv_rope(const void* const* w, void* const* y, const int
                                  const float* const* head_gamma, float head_eps, int pos, double rope_base,
                                  const void* x, const float* gamma, float eps, int64_t K, cudaStream_t s);
 
+// A sequence of one-token GEMV steps in one persistent cooperative launch
+// (jllm_q4k_gemv_chain): step s+1 reads x only after every y of step s is
+// written.  sync: n_steps + 1 zeroed words, left zeroed by a launch that
+// completes.  At most kChainMaxSteps steps of kChainMaxMats matrices, K at
+// most kChainMaxBlocks * 256.
+constexpr int kChainMaxSteps = 256;
+constexpr int kChainMaxMats = 4;
+constexpr int kChainMaxBlocks = 48;
+cudaError_t launch_gemv_chain(const jllm_gemv_step* steps, int n_steps, uint32_t* sync, cudaStream_t s);
+
 // TMA + tcgen05 GEMM for any M >= 1.  w1 != nullptr selects the SwiGLU
 // epilogue (y = fp16 h).  ws (nullptr allowed) of at least
 // gemm_workspace_bytes() zero-initialised bytes enables the stream-K split.
@@ -84,11 +96,13 @@ cudaError_t gemm_static_workspace_reset(cudaStream_t s);
 // Test builds only: make one bounded wait of the next launches run out.
 cudaError_t fault_injection_set_gemm(int skip_x);
 cudaError_t fault_injection_set_gemv(int skip_w);
+cudaError_t fault_injection_set_chain(int skip);
 #endif
 
 // Read and clear the device error word of the tcgen05 kernels (after
-// synchronising the stream) and of the GEMV kernels.
+// synchronising the stream), of the GEMV kernels and of the GEMV chain.
 cudaError_t read_clear_gemm_error(uint32_t* bits, cudaStream_t s);
 cudaError_t read_clear_gemv_error(uint32_t* bits);
+cudaError_t read_clear_chain_error(uint32_t* bits);
 
 }  // namespace jllm

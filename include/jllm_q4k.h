@@ -189,6 +189,55 @@ jllm_status jllm_q4k_gemv_qkv_rope(const void* const* w_q4k, float* const* y, in
                                    int64_t pos, float rope_base, jllm_stream_t stream);
 
 /*
+ * jllm_q4k_gemv_chain -- a sequence of decode GEMV steps in ONE persistent
+ * launch (one CTA per SM, all resident: a cooperative launch).  Step s is
+ * count (1..4) GEMVs over one x: y_i[n] = sum_k x[k] * w_i[n,k], n < N[i].
+ * The steps run in order: step s+1 reads its x only after every y of steps
+ * 0..s is written, so a step may read an earlier step's y (with y_f16 = 1
+ * it is directly an fp16 x).  Weights are streamed ahead of the steps,
+ * across step boundaries.  The pages name no such call: it is the decode
+ * sweep of the README's "INT4 dequant-fused GEMV" (At a glance, Kernels
+ * bullet) -- a layer's q/k/v, o, gate/up and down projections, layer after
+ * layer -- without a launch per matmul.
+ *   steps  : host array of n_steps (1..JLLM_CHAIN_MAX_STEPS) descriptors,
+ *            read before the call returns (the launch keeps a copy)
+ *     count  : 1..JLLM_CHAIN_MAX_MATS
+ *     y_f16  : 0 = y fp32, 1 = y fp16 (round to nearest even)
+ *     K      : a multiple of 256, at most JLLM_CHAIN_MAX_K
+ *     x      : [K] fp16, device, 16-byte aligned
+ *     w_q4k[i], y[i], N[i] : W_i [N[i]][K/256] blocks, its output [N[i]],
+ *            both device and 16-byte aligned; N[i] >= 0 (0: the entry is
+ *            skipped and its pointers are not read)
+ *   sync   : device, jllm_q4k_gemv_chain_sync_bytes(n_steps) bytes, 4-byte
+ *            aligned, zero before the first call (cudaMemset); a call that
+ *            completes leaves it zero.  One sync buffer serves one call at a
+ *            time (not two chains that may run concurrently).
+ * Each y equals jllm_q4k_gemv's within the matmul bound (the split of K and
+ * the summation order differ).  No W of any step may be written by an
+ * earlier step of the same call nor by the kernel enqueued just before it.
+ * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED, CUDA (also when the
+ *         device cannot hold one CTA per SM).  A bounded wait that runs out
+ *         is reported by jllm_get_device_error; sync must then be zeroed
+ *         again before the next call.
+ */
+#define JLLM_CHAIN_MAX_STEPS 256
+#define JLLM_CHAIN_MAX_MATS 4
+#define JLLM_CHAIN_MAX_K 12288
+typedef struct {
+  int32_t count;
+  int32_t y_f16;
+  int64_t K;
+  const void* x;
+  const void* w_q4k[JLLM_CHAIN_MAX_MATS];
+  void* y[JLLM_CHAIN_MAX_MATS];
+  int64_t N[JLLM_CHAIN_MAX_MATS];
+} jllm_gemv_step;
+jllm_status jllm_q4k_gemv_chain(const jllm_gemv_step* steps, int n_steps, uint32_t* sync, jllm_stream_t stream);
+
+/* Bytes of the sync buffer of a chain of n_steps steps (0 outside 1..JLLM_CHAIN_MAX_STEPS). */
+size_t jllm_q4k_gemv_chain_sync_bytes(int n_steps);
+
+/*
  * jllm_q4k_gemm -- Y[M,N] = X[M,K] * dequant(W)^T for any M >= 1.
  * (the README's "tensor-core MMQ Q4_K prefill" for M above the GEMV
  *  threshold, the GEMV kernel at or below it)

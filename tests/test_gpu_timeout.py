@@ -5,7 +5,8 @@ has a switch that makes one copy never be issued: CTA 0 of the tcgen05 GEMM
 skips its first X tile, or warp 0 of CTA 0 of the GEMV skips its weight
 rows.  The wait on that copy then runs out: the kernel must set its error
 word, wind down (copies and MMAs in flight awaited, tensor memory freed) and
-return, jllm_get_device_error must report JLLM_ERR_DEVICE_TIMEOUT, and the
+return (the GEMV chain: CTA 0's producer skips its first copy, and the other
+CTAs give up waiting for CTA 0's step counter), jllm_get_device_error must report JLLM_ERR_DEVICE_TIMEOUT, and the
 next calls on the same context must be correct again -- including
 jllm_q4k_gemm_noalloc, whose static workspace a timed-out call leaves with
 stale stream-K flags until jllm_get_device_error clears them.  Runs in a child
@@ -84,6 +85,38 @@ assert lib.jllm_test_fault_injection(0, 1) == 0
 assert gemv() == 0 and lib.jllm_get_device_error(s) == TIMEOUT
 assert lib.jllm_test_fault_injection(0, 0) == 0
 assert gemv() == 0 and lib.jllm_get_device_error(s) == 0 and within(y1.cpu().numpy()[None, :], r1, s1)
+
+# GEMV chain: the producer of CTA 0 never issues its first copy; the other CTAs
+# then give up waiting for CTA 0's step counter
+class Step(ctypes.Structure):
+    _fields_ = [("count", ctypes.c_int32), ("y_f16", ctypes.c_int32), ("K", ctypes.c_int64),
+                ("x", ctypes.c_void_p), ("w_q4k", ctypes.c_void_p * 4), ("y", ctypes.c_void_p * 4),
+                ("N", ctypes.c_int64 * 4)]
+lib.jllm_q4k_gemv_chain.argtypes = [ctypes.POINTER(Step), ctypes.c_int, P, P]
+lib.jllm_q4k_gemv_chain_sync_bytes.restype = ctypes.c_size_t
+lib.jllm_test_fault_injection_chain.argtypes = [ctypes.c_int]
+yc = torch.empty(N1, dtype=torch.float32, device="cuda")
+steps = (Step * 3)()
+for st in steps:
+    st.count, st.y_f16, st.K, st.x = 1, 0, K, x1d.data_ptr()
+    st.w_q4k[0], st.y[0], st.N[0] = w1d.data_ptr(), yc.data_ptr(), N1
+sync = torch.zeros(lib.jllm_q4k_gemv_chain_sync_bytes(3), dtype=torch.uint8, device="cuda")
+torch.cuda.synchronize()
+chain = lambda: lib.jllm_q4k_gemv_chain(steps, 3, sync.data_ptr(), s)
+assert chain() == 0 and lib.jllm_get_device_error(s) == 0 and within(yc.cpu().numpy()[None, :], r1, s1)
+for rnd in range(2):
+    assert lib.jllm_test_fault_injection_chain(1) == 0
+    t0 = time.time()
+    assert chain() == 0
+    st_ = lib.jllm_get_device_error(s)
+    assert st_ == TIMEOUT, st_
+    assert time.time() - t0 < 5.0
+    assert lib.jllm_test_fault_injection_chain(0) == 0
+    sync.zero_()  # the caller zeroes the sync words again after a timeout
+    yc.fill_(float("nan"))
+    assert chain() == 0 and lib.jllm_get_device_error(s) == 0
+    assert within(yc.cpu().numpy()[None, :], r1, s1), "chain after a timeout"
+    assert not sync.any().item()
 print("ok")
 '''
 
