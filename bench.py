@@ -890,7 +890,11 @@ def run_tc_rates(args):
     # (kind, name, CTAs, warps per CTA measured, ops per instruction, instructions per iteration per issuer)
     cases = ((0, "tcgen05_kind_f16", sms, 1, 2 * 128 * 256 * 16, 4),
              (1, "mma_sync_f16_m16n8k16", 2 * sms, 8, 2 * 16 * 8 * 16, 4),
-             (2, "mma_sync_s8_m16n8k32", 2 * sms, 8, 2 * 16 * 8 * 32, 4))
+             (2, "mma_sync_s8_m16n8k32", 2 * sms, 8, 2 * 16 * 8 * 32, 4),
+             # the tcgen05 stream with a commit per 4 MMAs, and a probe of a completed barrier phase
+             (5, "tcgen05_kind_f16_commit_per_4", sms, 1, 2 * 128 * 256 * 16, 4),
+             (3, "tcgen05_kind_f16_commit_try_wait_per_4", sms, 1, 2 * 128 * 256 * 16, 4),
+             (4, "tcgen05_kind_f16_commit_test_wait_per_4", sms, 1, 2 * 128 * 256 * 16, 4))
     for kind, name, ctas, wpc, ops, per_iter in cases:
         cyc = torch.zeros(ctas * wpc, dtype=torch.int64, device=dev)
         best = None
