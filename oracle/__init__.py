@@ -287,13 +287,17 @@ def tolerance(s: np.ndarray) -> np.ndarray:
 def swiglu_tolerance(g: np.ndarray, u: np.ndarray, sg: np.ndarray, su: np.ndarray) -> np.ndarray:
     """Per-element bound for a GPU h = fp16(silu(g') * u') whose g', u' each meet the matmul bound.
 
-    With Eg = tolerance(sg), Eu = tolerance(su) and |silu'| <= 1.1 everywhere:
-        |h' - silu(g)*u| <= 1.1*Eg*(|u| + Eu) + |silu(g)|*Eu + 2^-10*|silu(g)*u| + 1e-5
-    (the last two terms cover the fp32 evaluation and the rounding to fp16).
+    With Eg = tolerance(sg), Eu = tolerance(su) and |silu'| <= 1.1 everywhere, the exact
+    product of the perturbed inputs differs from silu(g)*u by at most
+        P = 1.1*Eg*(|u| + Eu) + |silu(g)|*Eu,
+    and the fp32 evaluation plus the rounding to fp16 add at most 2^-10 of its magnitude,
+    |silu(g)*u| + P, so
+        |h' - silu(g)*u| <= (1 + 2^-10)*P + 2^-10*|silu(g)*u| + 1e-5.
     """
     g = np.asarray(g, dtype=np.float64)
     u = np.asarray(u, dtype=np.float64)
     eg = tolerance(sg)
     eu = tolerance(su)
     sil = g / (1.0 + np.exp(-np.clip(g, -700, 700)))
-    return 1.1 * eg * (np.abs(u) + eu) + np.abs(sil) * eu + 2.0**-10 * np.abs(sil * u) + 1e-5
+    pert = 1.1 * eg * (np.abs(u) + eu) + np.abs(sil) * eu
+    return (1.0 + 2.0**-10) * pert + 2.0**-10 * np.abs(sil * u) + 1e-5

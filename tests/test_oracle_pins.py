@@ -341,6 +341,34 @@ def test_swiglu_against_closed_forms():
 
 # ------------------------------------------------------- synthetic inputs ----
 
+def test_swiglu_tolerance_covers_perturbed_inputs_and_is_not_loose():
+    """swiglu_tolerance against what it claims to bound: h' = fp16(silu(g')*u') for every
+    g', u' within the matmul bound of g, u (the four corners and random interior points of
+    the box), computed in fp64 and rounded to fp16; and not loose where silu' >= 1/2 (the
+    bound is within 3x of the largest deviation found there)."""
+    rng = np.random.Generator(np.random.PCG64(3))
+    n = 20000
+    g = rng.normal(0.0, 4.0, n)
+    u = rng.normal(0.0, 4.0, n)
+    u[:200] *= 1e-3  # |u| far below its own bound: the perturbed product dominates
+    sg = rng.uniform(0.0, 50.0, n)
+    su = rng.uniform(0.0, 50.0, n)
+    eg, eu = oracle.tolerance(sg), oracle.tolerance(su)
+    h = oracle.swiglu(g, u)
+    tol = oracle.swiglu_tolerance(g, u, sg, su)
+    worst = np.zeros(n)
+    deltas = [(a, b) for a in (-1.0, 1.0) for b in (-1.0, 1.0)]
+    deltas += [tuple(rng.uniform(-1.0, 1.0, 2)) for _ in range(8)]
+    for a, b in deltas:
+        hp = oracle.swiglu(g + a * eg, u + b * eu).astype(np.float16).astype(np.float64)
+        worst = np.maximum(worst, np.abs(hp - h))
+    assert np.all(worst <= tol)
+    sig = 1.0 / (1.0 + np.exp(-g))
+    steep = sig * (1.0 + g * (1.0 - sig)) >= 0.5
+    assert steep.sum() > 5000
+    assert np.all(tol[steep] <= 3.0 * worst[steep])
+
+
 def test_rmsnorm_against_closed_forms():
     # (3, 4): mean square 12.5, root 5/sqrt(2): outputs 3*sqrt(2)/5 and 4*sqrt(2)/5
     xn = oracle.rmsnorm(np.array([3.0, 4.0]), np.ones(2), 0.0)
