@@ -45,7 +45,7 @@
  * A launch failure returns JLLM_ERR_CUDA.  Kernel-side waits are bounded: a
  * wait that runs out sets a device error word that jllm_get_device_error()
  * reads.  No call throws or prints.  State kept: cached device properties,
- * the driver's tensor-map encoder, a table of the 64 most recently used
+ * the CUDA driver's tensor-map encoder, a table of the 64 most recently used
  * encoded tensor maps (keyed by device, address, extents and tile; guarded by
  * a mutex), and the static workspace of jllm_q4k_gemm_noalloc.  Environment variables read (once per process):
  * JLLM_PDL and JLLM_GEMV_MAX_M, described below; no other setting changes
