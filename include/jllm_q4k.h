@@ -212,6 +212,10 @@ jllm_status jllm_q4k_gemv_qkv_rope(const void* const* w_q4k, float* const* y, in
  *            aligned, zero before the first call (cudaMemset); a call that
  *            completes leaves it zero.  One sync buffer serves one call at a
  *            time (not two chains that may run concurrently).
+ * The launch holds one CTA on every SM (about 221 KiB of shared memory each)
+ * for its whole duration; CTAs wait on one another's step counters, so other
+ * work on the device can delay it (a wait that runs out after 2 s is reported
+ * by jllm_get_device_error) but not change its results.
  * Each y equals jllm_q4k_gemv's within the matmul bound (the split of K and
  * the summation order differ).  No W of any step may be written by an
  * earlier step of the same call nor by the kernel enqueued just before it.
