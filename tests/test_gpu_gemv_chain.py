@@ -159,3 +159,35 @@ def test_decode_sweep_full_size(q):
     for _, _, ys, _, _ in steps:  # every output written
         for y in ys:
             assert torch.isfinite(y).all().item()
+
+
+@pytest.mark.parametrize("seed", [21, 22, 23])
+def test_random_chains(q, seed):
+    """Random small chains: 1..12 steps, K from one to eleven blocks, 1..4 matrices of
+    0..700 rows, fp32 or fp16 outputs, every output against the oracle."""
+    import torch
+
+    rng = np.random.Generator(np.random.PCG64(seed))
+    steps, refs = [], []
+    for i in range(int(rng.integers(1, 13))):
+        K = 256 * int(rng.integers(1, 12))
+        cnt = int(rng.integers(1, 5))
+        Ns = [int(rng.integers(0, 701)) for _ in range(cnt)]
+        if sum(Ns) == 0:
+            Ns[0] = 1
+        f16 = bool(rng.integers(0, 2))
+        x = synthetic.activations(1, K, synthetic.activation_seed(seed, i, 0))
+        ws = [synthetic.q4k_weights(n, K, synthetic.weight_seed(seed, i, j)) if n
+              else np.zeros((0, K // 256 * 144), np.uint8) for j, n in enumerate(Ns)]
+        refs.append([oracle.matmul(w, x, n, K) if n else None for w, n in zip(ws, Ns)])
+        dt = torch.float16 if f16 else torch.float32
+        ys = [torch.full((max(n, 1),), float("nan"), dtype=dt, device="cuda")[:n] for n in Ns]
+        steps.append(([dev(w) for w in ws], dev(x.reshape(K)), ys, Ns, K))
+    q.GemvChain(steps)()
+    assert q.jllm_get_device_error() == 0
+    for i, (_, _, ys, Ns, K) in enumerate(steps):
+        for j, n in enumerate(Ns):
+            if n:
+                ref, s_ = refs[i][j]
+                y = ys[j].float().cpu().numpy()[None, :]
+                assert_within(y, ref, s_, f"seed {seed} step {i} matrix {j} (K {K}, N {n})")
