@@ -128,7 +128,12 @@ template <bool SWIGLU, bool ATMEM = false>
 struct Cfg {
   static constexpr int NMAT = SWIGLU ? 2 : 1;            // weight matrices per tile
   static constexpr int SX = ATMEM ? 6 : 3;               // X ring
-  static constexpr int SA = SWIGLU ? 3 : (ATMEM ? 8 : 4); // dequantised-A ring
+  // COMB: X and A share one stage index, one full barrier (the X copy and the 8
+  // dequant warps arrive on it) and one empty barrier (one commit per K step).
+  // Taken with A in tensor memory, where the A ring can match the X ring; with A
+  // in shared memory the shorter A ring it would need costs more than it saves.
+  static constexpr bool COMB = ATMEM;
+  static constexpr int SA = COMB ? SX : (SWIGLU ? 3 : 4); // dequantised-A ring
   static constexpr int SW = SWIGLU ? 2 : 3;              // raw-W ring
   static constexpr int BN_MAX = SWIGLU ? 128 : (ATMEM ? (int)ACC_COLS_ATMEM : 256);
   static constexpr uint32_t ACC = ATMEM ? ACC_COLS_ATMEM : ACC_COLS;  // TMEM columns per accumulator
@@ -256,6 +261,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t sbase = smem_u32(smem);
   const uint32_t sx = sbase + p.off_x, sa = sbase + p.off_a, sw = sbase + p.off_w;
   // barriers: x_full[SX] x_empty[SX] a_full[SA] a_empty[SA] w_full[SW] w_empty[SW]
+  //           (COMB: x_full / x_empty serve X and A; a_full / a_empty unused)
   //           acc_full[2] acc_empty[2] drain
   const uint32_t b_xfull = sbase + p.off_bar, b_xempty = b_xfull + 8 * SX;
   const uint32_t b_afull = b_xempty + 8 * SX, b_aempty = b_afull + 8 * SA;
@@ -268,7 +274,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < SX; ++i) {
-      mbar_init(b_xfull + 8 * i, 1);
+      mbar_init(b_xfull + 8 * i, C::COMB ? 9 : 1);  // COMB: the X copy and the 8 dequant warps
       mbar_init(b_xempty + 8 * i, 1);
     }
     for (int i = 0; i < SA; ++i) {
@@ -392,7 +398,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)racc.s * C::ACC;
         bool x_ready = mbar_test_wait(b_xfull + 8 * rx.s, rx.ph);
-        bool a_ready = mbar_test_wait(b_afull + 8 * ra.s, ra.ph);
+        bool a_ready = C::COMB || mbar_test_wait(b_afull + 8 * ra.s, ra.ph);
         for (int k = it.k0; k < it.k1; ++k) {
           if ((!x_ready && !wait(b_xfull + 8 * rx.s, rx.ph)) || (!a_ready && !wait(b_afull + 8 * ra.s, ra.ph))) {
             ok = false;
@@ -405,7 +411,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           rx.next();
           if (k + 1 < it.k1) {
             x_ready = mbar_test_wait(b_xfull + 8 * rx.s, rx.ph);
-            a_ready = mbar_test_wait(b_afull + 8 * ra.s, ra.ph);
+            a_ready = C::COMB || mbar_test_wait(b_afull + 8 * ra.s, ra.ph);
           }
           const uint32_t acc0 = k > it.k0 ? 1u : 0u;
           if (ATMEM) {
@@ -421,7 +427,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               if (SWIGLU) umma_f16(d + 128, ad + A2 + 2 * kk, bd + 2 * kk, idesc, 1u);
             }
           }
-          umma_commit(b_aempty + 8 * sa_now);
+          if (!C::COMB) umma_commit(b_aempty + 8 * sa_now);
           umma_commit(b_xempty + 8 * sx_now);
         }
         if (!ok) break;
@@ -450,7 +456,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int c = k & 3;
         // Waits are made warp-uniform so that a timeout leaves the warp converged.
         if (k == it.k0 || c == 0) ok = __all_sync(0xffffffffu, wait(b_wfull + 8 * rw.s, rw.ph));
-        if (ok) ok = __all_sync(0xffffffffu, wait(b_aempty + 8 * ra.s, ra.ph ^ 1u));
+        if (ok) ok = __all_sync(0xffffffffu, wait((C::COMB ? b_xempty : b_aempty) + 8 * ra.s, ra.ph ^ 1u));
         if (!ok) break;
 #pragma unroll
         for (int mat = 0; mat < NMAT; ++mat) {
@@ -496,7 +502,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (ATMEM) tc_fence_before();
         else fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(b_afull + 8 * ra.s);
+        if (lane == 0) mbar_arrive((C::COMB ? b_xfull : b_afull) + 8 * ra.s);
         ra.next();
         if (k == it.k1 - 1 || c == 3) {
           if (lane == 0) mbar_arrive(b_wempty + 8 * rw.s);
