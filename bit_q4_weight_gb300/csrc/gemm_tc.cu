@@ -122,12 +122,17 @@ constexpr uint64_t WAIT_LIMIT_NS = JLLM_WAIT_LIMIT_NS;  // 2 s (a test build sho
 // 64 fp16, two per 32-bit column).
 constexpr uint32_t ACC_COLS_ATMEM = 128;
 constexpr uint32_t A_TMEM_COL0 = 2 * ACC_COLS_ATMEM;  // first column of the A ring
-constexpr uint32_t A_TMEM_STAGE_COLS = KSTEP / 2;     // 32
 
 template <bool SWIGLU, bool ATMEM = false>
 struct Cfg {
   static constexpr int NMAT = SWIGLU ? 2 : 1;            // weight matrices per tile
-  static constexpr int SX = ATMEM ? 6 : 3;               // X ring
+  // K per pipeline step: 128 with A in tensor memory (two 64-wide X boxes and
+  // eight MMAs per synchronisation round), else 64 (one 128-byte swizzle atom
+  // of the A tile in shared memory).
+  static constexpr int KST = ATMEM ? 128 : KSTEP;
+  static constexpr int SPB = QK / KST;                   // steps per super-block
+  static constexpr uint32_t ASC = KST / 2;               // tensor-memory columns of an A stage
+  static constexpr int SX = ATMEM ? 4 : 3;               // X ring
   // COMB: X and A share one stage index, one full barrier (the X copy and the 8
   // dequant warps arrive on it) and one empty barrier (one commit per K step).
   // Taken with A in tensor memory, where the A ring can match the X ring; with A
@@ -138,7 +143,7 @@ struct Cfg {
   static constexpr int BN_MAX = SWIGLU ? 128 : (ATMEM ? (int)ACC_COLS_ATMEM : 256);
   static constexpr uint32_t ACC = ATMEM ? ACC_COLS_ATMEM : ACC_COLS;  // TMEM columns per accumulator
   static constexpr int NBARS = 2 * (SX + SA + SW) + 2 + 2 + 1;
-  static_assert(!ATMEM || (!SWIGLU && A_TMEM_COL0 + SA * A_TMEM_STAGE_COLS <= TMEM_COLS), "tensor memory budget");
+  static_assert(!ATMEM || (!SWIGLU && A_TMEM_COL0 + SA * ASC <= TMEM_COLS), "tensor memory budget");
 };
 
 // Up to kMaxGemmBatch weight matrices that share X (and so K) run in one
@@ -336,7 +341,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #endif
           {
             mbar_arrive_expect_tx(b_xfull + 8 * rx.s, p.x_stage_bytes);
-            tma_load_2d(sx + (uint32_t)rx.s * p.x_stage_bytes, &tmX, b_xfull + 8 * rx.s, k * KSTEP, m0);
+            // one 64-wide box per half of the step (the 128-byte swizzle atom)
+#pragma unroll
+            for (int h = 0; h < C::KST / KSTEP; ++h)
+              tma_load_2d(sx + (uint32_t)rx.s * p.x_stage_bytes + (uint32_t)(h * p.BN * KSTEP * 2), &tmX,
+                          b_xfull + 8 * rx.s, k * C::KST + h * KSTEP, m0);
           }
           rx.next();
           ++nx;
@@ -356,15 +365,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const TileLoc loc = locate(p, it.tile);
         const CUtensorMap* mw = &tmW.w[loc.b];
         for (int k = it.k0; k < it.k1; ++k) {
-          if (k == it.k0 || (k & 3) == 0) {
+          if (k == it.k0 || (k & (C::SPB - 1)) == 0) {
             if (!wait(b_wempty + 8 * rw.s, rw.ph ^ 1u)) {
               ok = false;
               break;
             }
             const uint32_t bar = b_wfull + 8 * rw.s;
             mbar_arrive_expect_tx(bar, W_STAGE_BYTES * NMAT);
-            tma_load_3d(sw + (uint32_t)(rw.s * NMAT) * W_STAGE_BYTES, mw, bar, 0, k >> 2, loc.n0);
-            if (SWIGLU) tma_load_3d(sw + (uint32_t)(rw.s * NMAT + 1) * W_STAGE_BYTES, &tmW.w[1], bar, 0, k >> 2, loc.n0);
+            tma_load_3d(sw + (uint32_t)(rw.s * NMAT) * W_STAGE_BYTES, mw, bar, 0, k / C::SPB, loc.n0);
+            if (SWIGLU)
+              tma_load_3d(sw + (uint32_t)(rw.s * NMAT + 1) * W_STAGE_BYTES, &tmW.w[1], bar, 0, k / C::SPB, loc.n0);
             rw.next();
             ++nw;
           }
@@ -415,9 +425,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           const uint32_t acc0 = k > it.k0 ? 1u : 0u;
           if (ATMEM) {
-            const uint32_t at = tmem + A_TMEM_COL0 + sa_now * A_TMEM_STAGE_COLS;
+            const uint32_t at = tmem + A_TMEM_COL0 + sa_now * C::ASC;
+            const uint32_t half = (uint32_t)(p.BN * KSTEP * 2) >> 4;  // second 64-wide X box of the step
 #pragma unroll
-            for (int kk = 0; kk < KSTEP / 16; ++kk) umma_f16_ta(d, at + 8 * kk, bd + 2 * kk, idesc, kk ? 1u : acc0);
+            for (int kk = 0; kk < C::KST / 16; ++kk)
+              umma_f16_ta(d, at + 8 * kk, bd + (kk >> 2) * half + 2 * (kk & 3), idesc, kk ? 1u : acc0);
           } else {
             umma_f16(d, ad, bd, idesc, acc0);
             if (SWIGLU) umma_f16(d + 128, ad + A2, bd, idesc, acc0);
@@ -440,22 +452,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else if (warp < EPI_WARP0) {
     // --------------------------------------------------------------- dequant --
-    // Warp w handles TMEM lane quarter q = w & 3 (rows 32q..32q+31) and nibble
-    // side hs = (w - 2) >> 2: hs = 0 makes sub-block 2c (low nibbles, k 0..31
-    // of the step), hs = 1 sub-block 2c+1 (high nibbles, k 32..63).
+    // Warp w handles TMEM lane quarter q = w & 3 (rows 32q..32q+31) and half
+    // hw = (w - 2) >> 2 of each step.  64-wide steps: hw is the nibble side --
+    // hw = 0 makes sub-block 2c (low nibbles, k 0..31 of the step), hw = 1
+    // sub-block 2c+1 (high nibbles, k 32..63).  128-wide steps: hw is the
+    // 64-weight chunk of the step, and the warp makes both of its sub-blocks.
     const int q = warp & 3;
-    const int hs = (warp - 2) >> 2;
+    const int hw = (warp - 2) >> 2;
     const int r = 32 * q + lane;
-    const uint32_t mask = hs ? 0x00F000F0u : 0x000F000Fu;
+    constexpr int NH = C::KST / KSTEP;  // sub-block halves per thread and step
     Ring<SA> ra;
     Ring<SW> rw;
     bool ok = true;
     UnitIter it{u_begin, u_end, p.KS};
     while (ok && it.next()) {
       for (int k = it.k0; k < it.k1; ++k) {
-        const int c = k & 3;
+        const int ks = k & (C::SPB - 1);  // step within the super-block
+        const int c = NH == 2 ? 2 * ks + hw : ks;  // this thread's 64-weight chunk of the block
         // Waits are made warp-uniform so that a timeout leaves the warp converged.
-        if (k == it.k0 || c == 0) ok = __all_sync(0xffffffffu, wait(b_wfull + 8 * rw.s, rw.ph));
+        if (k == it.k0 || ks == 0) ok = __all_sync(0xffffffffu, wait(b_wfull + 8 * rw.s, rw.ph));
         if (ok) ok = __all_sync(0xffffffffu, wait((C::COMB ? b_xempty : b_aempty) + 8 * ra.s, ra.ph ^ 1u));
         if (!ok) break;
 #pragma unroll
@@ -464,38 +479,46 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint4 hd = *reinterpret_cast<const uint4*>(raw);
           const uint4 q0 = *reinterpret_cast<const uint4*>(raw + 16 + 32 * c);
           const uint4 q1 = *reinterpret_cast<const uint4*>(raw + 32 + 32 * c);
-          uint32_t sc, m;
-          q4k_scale_min(hd.y, hd.z, hd.w, 2 * c + hs, sc, m);
-          // p = sc*q exactly in fp16 from the offset code h (1024+q or 1024+16q):
-          //   p = h*sc - 1024*sc  or  p = h*(sc/16) - 64*sc   (one rounding of an
-          //   exact integer <= 945).  Then w = fma(d, p, -dmin*m) in fp32 is the
-          //   exact value rounded once, i.e. the fp32 dequant, rounded to fp16.
-          const __half sch = __uint2half_rn(sc);
-          const __half2 scv = __half2half2(hs ? __hmul(sch, __float2half(0.0625f)) : sch);
-          const __half2 offv = __half2half2(__hmul(sch, __float2half(hs ? -64.f : -1024.f)));
-          const uint32_t scv_u = *reinterpret_cast<const uint32_t*>(&scv);
-          const uint32_t offv_u = *reinterpret_cast<const uint32_t*>(&offv);
           const unsigned short d16 = (unsigned short)(hd.x & 0xffffu);
-          const float nt = -__fmul_rn(half_hi_to_float(hd.x), (float)m);
           const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-          uint32_t pk[16];  // fp16 pairs (k, k+1) for k = 32*hs + 2*i of the step
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            uint32_t wp;
-            asm("prmt.b32 %0, %1, 0, 0x3120;" : "=r"(wp) : "r"(qw[i]));  // bytes b0 b2 b1 b3
-            pk[2 * i] = dq_pair(lop3_and_or(wp, mask, 0x64006400u), scv_u, offv_u, d16, nt);           // k, k+1
-            pk[2 * i + 1] = dq_pair(lop3_and_or(wp >> 8, mask, 0x64006400u), scv_u, offv_u, d16, nt);  // k+2, k+3
-          }
-          if (ATMEM) {
-            // lane r of the warp's TMEM quarter, 16 columns of the step's 32 (two fp16 per column)
-            tmem_st16(tmem + ((uint32_t)(32 * q) << 16) + A_TMEM_COL0 + ra.s * A_TMEM_STAGE_COLS + 16 * hs, pk);
-          } else {
-            uint8_t* arow = smem + p.off_a + (size_t)(ra.s * NMAT + mat) * A_STAGE_BYTES + (size_t)r * 128;
+          for (int hi = 0; hi < NH; ++hi) {
+            const int hs = NH == 2 ? hi : hw;  // nibble side: sub-block 2c + hs
+            uint32_t sc, m;
+            q4k_scale_min(hd.y, hd.z, hd.w, 2 * c + hs, sc, m);
+            // p = sc*q exactly in fp16 from the offset code h (1024+q or 1024+16q):
+            //   p = h*sc - 1024*sc  or  p = h*(sc/16) - 64*sc   (one rounding of an
+            //   exact integer <= 945).  Then w = fma(d, p, -dmin*m) in fp32 is the
+            //   exact value rounded once, i.e. the fp32 dequant, rounded to fp16.
+            const uint32_t mask = hs ? 0x00F000F0u : 0x000F000Fu;
+            const __half sch = __uint2half_rn(sc);
+            const __half2 scv = __half2half2(hs ? __hmul(sch, __float2half(0.0625f)) : sch);
+            const __half2 offv = __half2half2(__hmul(sch, __float2half(hs ? -64.f : -1024.f)));
+            const uint32_t scv_u = *reinterpret_cast<const uint32_t*>(&scv);
+            const uint32_t offv_u = *reinterpret_cast<const uint32_t*>(&offv);
+            const float nt = -__fmul_rn(half_hi_to_float(hd.x), (float)m);
+            uint32_t pk[16];  // fp16 pairs (k, k+1) for k = 32*hs + 2*i of the chunk
 #pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {  // output chunk j8 = 4*hs + jj holds k = 8*j8..8*j8+7
-              const int j8 = 4 * hs + jj;
-              *reinterpret_cast<uint4*>(arow + ((j8 ^ (r & 7)) << 4)) =
-                  make_uint4(pk[4 * jj], pk[4 * jj + 1], pk[4 * jj + 2], pk[4 * jj + 3]);
+            for (int i = 0; i < 8; ++i) {
+              uint32_t wp;
+              asm("prmt.b32 %0, %1, 0, 0x3120;" : "=r"(wp) : "r"(qw[i]));  // bytes b0 b2 b1 b3
+              pk[2 * i] = dq_pair(lop3_and_or(wp, mask, 0x64006400u), scv_u, offv_u, d16, nt);           // k, k+1
+              pk[2 * i + 1] = dq_pair(lop3_and_or(wp >> 8, mask, 0x64006400u), scv_u, offv_u, d16, nt);  // k+2, k+3
+            }
+            if (ATMEM) {
+              // lane r of the warp's TMEM quarter, 16 columns of the stage (two fp16 per column):
+              // the chunk's 32 columns at 32*hw (128-wide steps), the sub-block's half at 16*hs
+              tmem_st16(tmem + ((uint32_t)(32 * q) << 16) + A_TMEM_COL0 + ra.s * C::ASC + (NH == 2 ? 32 * hw : 0) +
+                            16 * hs,
+                        pk);
+            } else {
+              uint8_t* arow = smem + p.off_a + (size_t)(ra.s * NMAT + mat) * A_STAGE_BYTES + (size_t)r * 128;
+#pragma unroll
+              for (int jj = 0; jj < 4; ++jj) {  // output chunk j8 = 4*hs + jj holds k = 8*j8..8*j8+7
+                const int j8 = 4 * hs + jj;
+                *reinterpret_cast<uint4*>(arow + ((j8 ^ (r & 7)) << 4)) =
+                    make_uint4(pk[4 * jj], pk[4 * jj + 1], pk[4 * jj + 2], pk[4 * jj + 3]);
+              }
             }
           }
         }
@@ -504,7 +527,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive((C::COMB ? b_xfull : b_afull) + 8 * ra.s);
         ra.next();
-        if (k == it.k1 - 1 || c == 3) {
+        if (k == it.k1 - 1 || ks == C::SPB - 1) {
           if (lane == 0) mbar_arrive(b_wempty + 8 * rw.s);
           rw.next();
         }
@@ -885,7 +908,8 @@ cudaError_t launch_tc_common(const void* const* w, const void* w1, const int64_t
     BN = (int)(((M + 1) / 2 + 15) / 16 * 16);
   // Tiles of at most 128 tokens keep the dequantised A operand in tensor memory
   // (9-12 % faster than in shared memory at the same tile width, measured at 128
-  // and 192 tokens); wider tiles need all 512 columns for two accumulators.
+  // and 192 tokens), with 128-wide K steps; wider tiles need all 512 columns for
+  // two accumulators.
   const bool atmem = !swiglu && kn.atmem != 0 && BN <= 128;
 
   GemmParams p = {};
@@ -893,7 +917,8 @@ cudaError_t launch_tc_common(const void* const* w, const void* w1, const int64_t
   p.NB = (int)(K / QK);
   p.BN = BN;
   p.m_tiles = (int)((M + BN - 1) / BN);
-  p.KS = 4 * p.NB;
+  const int kst = atmem ? Cfg<false, true>::KST : KSTEP;  // K per pipeline step
+  p.KS = (QK / kst) * p.NB;
   p.out_f16 = (y_f16 || swiglu) ? 1 : 0;
   p.count = count;
   long long tiles = 0;
@@ -935,7 +960,7 @@ cudaError_t launch_tc_common(const void* const* w, const void* w1, const int64_t
   const int SA = swiglu ? Cfg<true>::SA : (atmem ? Cfg<false, true>::SA : Cfg<false>::SA);
   const int SW = swiglu ? Cfg<true>::SW : (atmem ? Cfg<false, true>::SW : Cfg<false>::SW);
   const int nbars = swiglu ? Cfg<true>::NBARS : (atmem ? Cfg<false, true>::NBARS : Cfg<false>::NBARS);
-  p.x_stage_bytes = (uint32_t)BN * KSTEP * 2;
+  p.x_stage_bytes = (uint32_t)BN * kst * 2;
   p.off_x = 0;
   p.off_a = (uint32_t)SX * p.x_stage_bytes;
   p.off_w = p.off_a + (atmem ? 0u : (uint32_t)(SA * nmat * A_STAGE_BYTES));
