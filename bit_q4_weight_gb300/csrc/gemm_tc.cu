@@ -22,8 +22,9 @@
 //   warp 0      TMA producer: per K step one X tile {64 k x BN tokens},
 //               128-byte swizzled; per 256-wide block one raw W tile
 //               {144 bytes x 1 block x 128 rows} through a 3-D byte view.
-//   warp 1      TMEM owner (512 columns = two accumulator buffers) and MMA
-//               issuer (one thread): four tcgen05.mma (K = 16) per K step,
+//   warp 1      TMEM owner (512 columns = two accumulator buffers, or one
+//               for tiles of more than 256 tokens) and MMA issuer (one
+//               thread): four tcgen05.mma (K = 16) per K step and token half,
 //               tcgen05.commit frees the stages and, per unit, hands the
 //               accumulator buffer to the epilogue.
 //   warps 2-9   dequantisers, two threads per weight row (low / high nibbles
@@ -33,7 +34,8 @@
 //               layout the MMA descriptor reads.
 //   warps 10-13 epilogue: tcgen05.ld of one TMEM lane quarter, store Y
 //               (fp32 / fp16) or silu(g)*u (fp16), or the fp32 partial of a
-//               cut tile.  It runs while the MMA fills the other buffer.
+//               cut tile.  It runs while the MMA fills the other buffer (or,
+//               with one buffer, the half already drained).
 // Ring positions advance by counters (stage, phase), never by division.
 // Programmatic dependent launch: setup and the first weight blocks overlap
 // the previous kernel in the stream; X is loaded and Y, the partials and the
@@ -109,7 +111,7 @@ constexpr int EPI_WARP0 = 10;                       // warps 10..13
 constexpr int NUM_EPI_WARPS = 4;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COLS = 256;                  // TMEM columns per accumulator buffer
-constexpr int SLOT_FLOATS = TILE_N * 256;           // fp32 partial of one tile (128 KiB)
+constexpr int SLOT_FLOATS = TILE_N * 512;           // fp32 partial of one tile (256 KiB)
 #ifndef JLLM_WAIT_LIMIT_NS
 #define JLLM_WAIT_LIMIT_NS 2000000000ull
 #endif
@@ -123,7 +125,13 @@ constexpr uint64_t WAIT_LIMIT_NS = JLLM_WAIT_LIMIT_NS;  // 2 s (a test build sho
 constexpr uint32_t ACC_COLS_ATMEM = 128;
 constexpr uint32_t A_TMEM_COL0 = 2 * ACC_COLS_ATMEM;  // first column of the A ring
 
-template <bool SWIGLU, bool ATMEM = false>
+// WIDE: tiles of up to 512 tokens for long prompts.  Each K = 16 slice takes
+// two MMAs of BN/2 tokens (the two halves of the X stage) into one accumulator
+// of all 512 tensor-memory columns (half h at column 256*h), so a dequantised
+// weight meets twice the tokens per synchronisation round.  The epilogue
+// releases the halves one at a time, and the next tile's first MMAs into half
+// 0 start while half 1 is still being drained.
+template <bool SWIGLU, bool ATMEM = false, bool WIDE = false>
 struct Cfg {
   static constexpr int NMAT = SWIGLU ? 2 : 1;            // weight matrices per tile
   // K per pipeline step: 128 with A in tensor memory (two 64-wide X boxes and
@@ -132,18 +140,21 @@ struct Cfg {
   static constexpr int KST = ATMEM ? 128 : KSTEP;
   static constexpr int SPB = QK / KST;                   // steps per super-block
   static constexpr uint32_t ASC = KST / 2;               // tensor-memory columns of an A stage
-  static constexpr int SX = ATMEM ? 4 : 3;               // X ring
+  static constexpr int SX = ATMEM ? 4 : (WIDE ? 2 : 3);  // X ring
   // COMB: X and A share one stage index, one full barrier (the X copy and the 8
   // dequant warps arrive on it) and one empty barrier (one commit per K step).
   // Taken with A in tensor memory, where the A ring can match the X ring; with A
   // in shared memory the shorter A ring it would need costs more than it saves.
   static constexpr bool COMB = ATMEM;
-  static constexpr int SA = COMB ? SX : (SWIGLU ? 3 : 4); // dequantised-A ring
-  static constexpr int SW = SWIGLU ? 2 : 3;              // raw-W ring
-  static constexpr int BN_MAX = SWIGLU ? 128 : (ATMEM ? (int)ACC_COLS_ATMEM : 256);
-  static constexpr uint32_t ACC = ATMEM ? ACC_COLS_ATMEM : ACC_COLS;  // TMEM columns per accumulator
+  static constexpr int SA = COMB ? SX : (SWIGLU || WIDE ? 3 : 4);  // dequantised-A ring
+  static constexpr int SW = SWIGLU || WIDE ? 2 : 3;      // raw-W ring
+  static constexpr int XH = WIDE ? 2 : 1;                // token halves (X boxes, MMAs) per K slice
+  static constexpr int NACC = WIDE ? 1 : 2;              // accumulator buffers
+  static constexpr int BN_MAX = SWIGLU ? 128 : (ATMEM ? (int)ACC_COLS_ATMEM : (WIDE ? 512 : 256));
+  static constexpr uint32_t ACC = ATMEM ? ACC_COLS_ATMEM : (WIDE ? TMEM_COLS : ACC_COLS);  // TMEM columns per accumulator
   static constexpr int NBARS = 2 * (SX + SA + SW) + 2 + 2 + 1;
   static_assert(!ATMEM || (!SWIGLU && A_TMEM_COL0 + SA * ASC <= TMEM_COLS), "tensor memory budget");
+  static_assert(!WIDE || (!SWIGLU && !ATMEM), "wide tiles: one plain matrix, A in shared memory");
 };
 
 // Up to kMaxGemmBatch weight matrices that share X (and so K) run in one
@@ -158,7 +169,8 @@ struct GemmParams {
   float* partial;        // stream-K slots, SLOT_FLOATS per CTA (nullptr: whole tiles only)
   uint32_t* flags;       // one counter per CTA next to the slots
   int M, NB;
-  int BN;                // tokens per tile, multiple of 16
+  int BN;                // tokens per tile, multiple of 16 (of 64 for wide tiles)
+  int HB;                // tokens per MMA and X box: BN, or BN / 2 for wide tiles
   int m_tiles;           // ceil(M / BN)
   int KS;                // K steps per tile (4 per super-block)
   long long grains;      // units / grain
@@ -255,11 +267,11 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-template <bool SWIGLU, bool ATMEM>
+template <bool SWIGLU, bool ATMEM, bool WIDE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     q4k_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ WMaps tmW,
                        const __grid_constant__ GemmParams p) {
-  using C = Cfg<SWIGLU, ATMEM>;
+  using C = Cfg<SWIGLU, ATMEM, WIDE>;
   constexpr int NMAT = C::NMAT, SX = C::SX, SA = C::SA, SW = C::SW;
   extern __shared__ uint8_t gemm_smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(gemm_smem_raw) + 1023) & ~uintptr_t(1023));
@@ -341,11 +353,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #endif
           {
             mbar_arrive_expect_tx(b_xfull + 8 * rx.s, p.x_stage_bytes);
-            // one 64-wide box per half of the step (the 128-byte swizzle atom)
+            // one box of 64 k (the 128-byte swizzle atom) x HB tokens per K half
+            // and token half of the step
 #pragma unroll
             for (int h = 0; h < C::KST / KSTEP; ++h)
-              tma_load_2d(sx + (uint32_t)rx.s * p.x_stage_bytes + (uint32_t)(h * p.BN * KSTEP * 2), &tmX,
-                          b_xfull + 8 * rx.s, k * C::KST + h * KSTEP, m0);
+#pragma unroll
+              for (int t = 0; t < C::XH; ++t)
+                tma_load_2d(sx + (uint32_t)rx.s * p.x_stage_bytes + (uint32_t)((h * C::XH + t) * p.HB * KSTEP * 2),
+                            &tmX, b_xfull + 8 * rx.s, k * C::KST + h * KSTEP, m0 + t * p.HB);
           }
           rx.next();
           ++nx;
@@ -391,16 +406,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // in the start-address field, which cannot carry within shared memory),
       // and the barriers of step k+1 are probed (non-blocking test) before step
       // k's MMAs are issued so that the probe's latency overlaps the issue.
-      const uint32_t idesc = umma_idesc_f16(TILE_N, p.BN);
+      const uint32_t idesc = umma_idesc_f16(TILE_N, p.HB);
       const uint64_t adesc0 = umma_desc_sw128(sa), bdesc0 = umma_desc_sw128(sx);
       const uint32_t a_step = (uint32_t)(NMAT * A_STAGE_BYTES) >> 4, b_step = p.x_stage_bytes >> 4;
       constexpr uint32_t A2 = (uint32_t)A_STAGE_BYTES >> 4;  // second matrix of a SwiGLU stage
+      const uint32_t xhalf = (uint32_t)(p.HB * KSTEP * 2) >> 4;  // second token half of a wide X stage
       Ring<SA> ra;
       Ring<SX> rx;
-      Ring<2> racc;
+      Ring<C::NACC> racc;
       bool ok = true;
       UnitIter it{u_begin, u_end, p.KS};
       while (ok && it.next()) {
+        // (wide tiles: this is half 0; half 1 is awaited before its first MMA)
         if (!wait(b_accempty + 8 * racc.s, racc.ph ^ 1u)) {
           ok = false;
           break;
@@ -431,13 +448,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int kk = 0; kk < C::KST / 16; ++kk)
               umma_f16_ta(d, at + 8 * kk, bd + (kk >> 2) * half + 2 * (kk & 3), idesc, kk ? 1u : acc0);
           } else {
-            umma_f16(d, ad, bd, idesc, acc0);
-            if (SWIGLU) umma_f16(d + 128, ad + A2, bd, idesc, acc0);
 #pragma unroll
-            for (int kk = 1; kk < KSTEP / 16; ++kk) {
-              umma_f16(d, ad + 2 * kk, bd + 2 * kk, idesc, 1u);
-              if (SWIGLU) umma_f16(d + 128, ad + A2 + 2 * kk, bd + 2 * kk, idesc, 1u);
+            for (int t = 0; t < C::XH; ++t) {
+              if (WIDE && t == 1 && k == it.k0 && !wait(b_accempty + 8, racc.ph ^ 1u)) {
+                ok = false;
+                break;
+              }
+              if (WIDE && t == 1 && k == it.k0) tc_fence_after();
+              const uint32_t dt = d + 256u * t;
+              const uint64_t bt = bd + t * xhalf;
+              umma_f16(dt, ad, bt, idesc, acc0);
+              if (SWIGLU) umma_f16(dt + 128, ad + A2, bt, idesc, acc0);
+#pragma unroll
+              for (int kk = 1; kk < KSTEP / 16; ++kk) {
+                umma_f16(dt, ad + 2 * kk, bt + 2 * kk, idesc, 1u);
+                if (SWIGLU) umma_f16(dt + 128, ad + A2 + 2 * kk, bt + 2 * kk, idesc, 1u);
+              }
             }
+            if (!ok) break;
           }
           if (!C::COMB) umma_commit(b_aempty + 8 * sa_now);
           umma_commit(b_xempty + 8 * sx_now);
@@ -540,7 +568,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int q = warp & 3;
     const int r = 32 * q + lane;
     pdl_wait();  // Y, the partial slots and the flags are touched only after the previous kernel
-    Ring<2> racc;
+    Ring<C::NACC> racc;
+    // TMEM column of the tile's token column cc (a multiple of 32): wide tiles
+    // keep their second token half at column 256.
+    auto tcol = [&](int cc) -> uint32_t { return (uint32_t)(WIDE && cc >= p.HB ? 256 + cc - p.HB : cc); };
+    // This warp is done reading accumulator buffer (wide tiles: half) i.
+    auto release = [&](int i) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(b_accempty + 8 * i);
+    };
     bool ok = true;
     UnitIter it{u_begin, u_end, p.KS};
     while (ok && it.next()) {
@@ -554,20 +591,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const bool fixer = !writer && it.k1 < p.KS;      // first part of a cut tile
       constexpr int MAT_COLS = SWIGLU ? 128 : 0;       // TMEM column offset of the second matrix
       if (writer) {
-        // Leave the fp32 partial in this CTA's slot ([column][row], coalesced
-        // over rows), then count this warp in the slot's flag.
-        float* slot = p.partial + (size_t)blockIdx.x * SLOT_FLOATS;
+        // Leave the fp32 partial in this CTA's slot, then count this warp in
+        // the slot's flag.  Slot layout [column / 4][row][column % 4]: a warp
+        // moves 16 bytes per row, 512 contiguous bytes per access.
+        float4* slot = reinterpret_cast<float4*>(p.partial + (size_t)blockIdx.x * SLOT_FLOATS) + r;
         for (int mat = 0; mat < NMAT; ++mat) {
           for (int cc = 0; cc < p.BN; cc += 32) {
             uint32_t v[32];
-            tmem_ld32(tl + mat * MAT_COLS + cc, v);
+            tmem_ld32(tl + mat * MAT_COLS + tcol(cc), v);
+            if (WIDE && cc + 32 == p.HB) release(0);  // half 0 is in registers
 #pragma unroll
-            for (int j = 0; j < 32; ++j) __stcg(slot + (size_t)(mat * MAT_COLS + cc + j) * TILE_N + r, __uint_as_float(v[j]));
+            for (int i = 0; i < 8; ++i)
+              __stcg(slot + (size_t)((mat * MAT_COLS + cc) / 4 + i) * TILE_N,
+                     make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                 __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3])));
           }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(b_accempty + 8 * racc.s);
+        release(WIDE ? 1 : racc.s);
         __threadfence();
         __syncwarp();
         if (lane == 0) atom_add_release_gpu(p.flags + blockIdx.x, 1u);
@@ -592,16 +632,56 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           if (!ok) break;
         }
+        // The contributors' partial sums, added in CTA order.  Wide tiles: the
+        // sums of chunk cc + 32 are loaded before chunk cc's stores, so that
+        // their latency overlaps the stores and the next tensor-memory read
+        // (the other variants have no registers to spare for it).
+        const bool summed = j_end > (int)blockIdx.x + 1;
+        const float4* slot0 = reinterpret_cast<const float4*>(p.partial + (size_t)(blockIdx.x + 1) * SLOT_FLOATS) + r;
+        constexpr size_t SLOT4 = SLOT_FLOATS / 4;
+        float4 nx[8];
+        if (WIDE && summed) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) nx[i] = __ldcg(slot0 + (size_t)i * TILE_N);
+          for (int jc = blockIdx.x + 2; jc < j_end; ++jc)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float4 t = __ldcg(slot0 + (size_t)(jc - blockIdx.x - 1) * SLOT4 + (size_t)i * TILE_N);
+              nx[i].x += t.x, nx[i].y += t.y, nx[i].z += t.z, nx[i].w += t.w;
+            }
+        }
         for (int cc = 0; cc < p.BN; cc += 32) {
           uint32_t v[32];
-          tmem_ld32(tl + cc, v);
+          tmem_ld32(tl + tcol(cc), v);
+          if (WIDE && cc + 32 == p.HB) release(0);  // half 0 is in registers
           float a[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) a[j] = __uint_as_float(v[j]);
-          for (int jc = blockIdx.x + 1; jc < j_end; ++jc) {
-            const float* slot = p.partial + (size_t)jc * SLOT_FLOATS + (size_t)cc * TILE_N + r;
+          if (!WIDE) {
+            for (int jc = blockIdx.x + 1; jc < j_end; ++jc) {
+              const float4* slot = reinterpret_cast<const float4*>(p.partial + (size_t)jc * SLOT_FLOATS) +
+                                   (size_t)(cc / 4) * TILE_N + r;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) a[j] += __ldcg(slot + (size_t)j * TILE_N);
+              for (int i = 0; i < 8; ++i) {
+                const float4 t = __ldcg(slot + (size_t)i * TILE_N);
+                a[4 * i] += t.x, a[4 * i + 1] += t.y, a[4 * i + 2] += t.z, a[4 * i + 3] += t.w;
+              }
+            }
+          } else if (summed) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              a[4 * i] += nx[i].x, a[4 * i + 1] += nx[i].y, a[4 * i + 2] += nx[i].z, a[4 * i + 3] += nx[i].w;
+            if (cc + 32 < p.BN) {
+              const float4* slot = slot0 + (size_t)((cc + 32) / 4) * TILE_N;
+#pragma unroll
+              for (int i = 0; i < 8; ++i) nx[i] = __ldcg(slot + (size_t)i * TILE_N);
+              for (int jc = blockIdx.x + 2; jc < j_end; ++jc)
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                  const float4 t = __ldcg(slot + (size_t)(jc - blockIdx.x - 1) * SLOT4 + (size_t)i * TILE_N);
+                  nx[i].x += t.x, nx[i].y += t.y, nx[i].z += t.z, nx[i].w += t.w;
+                }
+            }
           }
           if (SWIGLU) {
             tmem_ld32(tl + MAT_COLS + cc, v);
@@ -609,17 +689,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
             for (int j = 0; j < 32; ++j) u[j] = __uint_as_float(v[j]);
             for (int jc = blockIdx.x + 1; jc < j_end; ++jc) {
-              const float* slot = p.partial + (size_t)jc * SLOT_FLOATS + (size_t)(MAT_COLS + cc) * TILE_N + r;
+              const float4* slot = reinterpret_cast<const float4*>(p.partial + (size_t)jc * SLOT_FLOATS) +
+                                   (size_t)((MAT_COLS + cc) / 4) * TILE_N + r;
 #pragma unroll
-              for (int j = 0; j < 32; ++j) u[j] += __ldcg(slot + (size_t)j * TILE_N);
+              for (int i = 0; i < 8; ++i) {
+                const float4 t = __ldcg(slot + (size_t)i * TILE_N);
+                u[4 * i] += t.x, u[4 * i + 1] += t.y, u[4 * i + 2] += t.z, u[4 * i + 3] += t.w;
+              }
             }
 #pragma unroll
             for (int j = 0; j < 32; ++j) a[j] = a[j] / (1.0f + expf(-a[j])) * u[j];  // h = silu(g) * u
           }
-          // Y[m0+cc+j][n] for the j in range: one pointer step of N per token, the
-          // bounds tested once per chunk.
           const int jv = min(32, min(p.BN - cc, p.M - (m0 + cc)));
           if (n < loc.N && jv > 0) {
+            // Y[m0+cc+j][n] for the j in range: one pointer step of N per token, the
+            // bounds tested once per chunk.
             const size_t off = (size_t)(m0 + cc) * loc.N + n;
             const size_t ld = (size_t)loc.N;
             if (p.out_f16) {
@@ -645,10 +729,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
           }
         }
-        tc_fence_before();
-        __syncwarp();
+        release(WIDE ? 1 : racc.s);
         if (lane == 0) {
-          mbar_arrive(b_accempty + 8 * racc.s);
           // The last of the four epilogue warps to finish returns the
           // contributors' flags to zero for the next call.
           for (int jc = blockIdx.x + 1; jc < j_end; ++jc)
@@ -778,10 +860,13 @@ cudaError_t make_w_map(const void* w, int64_t N, int64_t K, CUtensorMap* mw) {
 // overrides once from the environment (JLLM_GEMM_BN, JLLM_GEMM_SPLIT), for
 // measurements only.
 //   atmem  1: the A operand in tensor memory (single-GEMM and batched launches)
+//   wide   1: tiles of up to 512 tokens when M > 256 and they fill the SMs
+//          (single-GEMM and batched); 2: whenever M > 256
 struct GemmKnobs {
   int bn = 0;
   int split = 1;
   int atmem = 1;
+  int wide = 1;
 };
 const GemmKnobs& gemm_knobs() {
   static GemmKnobs k = [] {
@@ -790,16 +875,17 @@ const GemmKnobs& gemm_knobs() {
     if (const char* e = getenv("JLLM_GEMM_BN")) v.bn = atoi(e);
     if (const char* e = getenv("JLLM_GEMM_SPLIT")) v.split = atoi(e);
     if (const char* e = getenv("JLLM_GEMM_ATMEM")) v.atmem = atoi(e);
+    if (const char* e = getenv("JLLM_GEMM_WIDE")) v.wide = atoi(e);
 #endif
     return v;
   }();
   return k;
 }
 
-template <bool SWIGLU, bool ATMEM>
+template <bool SWIGLU, bool ATMEM, bool WIDE = false>
 cudaError_t launch_tc(const CUtensorMap& mx, const WMaps& mw, const GemmParams& p, int grid, bool cooperative,
                       size_t smem, cudaStream_t s) {
-  auto kern = q4k_gemm_tc_kernel<SWIGLU, ATMEM>;
+  auto kern = q4k_gemm_tc_kernel<SWIGLU, ATMEM, WIDE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -910,12 +996,28 @@ cudaError_t launch_tc_common(const void* const* w, const void* w1, const int64_t
   // (9-12 % faster than in shared memory at the same tile width, measured at 128
   // and 192 tokens), with 128-wide K steps; wider tiles need all 512 columns for
   // two accumulators.
-  const bool atmem = !swiglu && kn.atmem != 0 && BN <= 128;
+  const bool atmem = !swiglu && kn.atmem != 0 && BN <= Cfg<false, true>::BN_MAX;
+  // More than 256 tokens: wide tiles of up to 512 (the fewest tiles of at most
+  // 512 tokens, each a multiple of 64, so that the halves are multiples of 32),
+  // when there are at least as many as SMs.  Fewer would leave SMs idle or be
+  // cut between CTAs, and a cut wide tile's fix-up (256 KiB of partial sums per
+  // contributor) costs more than the wide tile saves.
+  using CW = Cfg<false, false, true>;
+  bool wide = false;
+  if (!swiglu && kn.wide != 0 && kn.bn == 0 && M > 256) {
+    const int64_t mt = (M + CW::BN_MAX - 1) / CW::BN_MAX;
+    if (mt * n_tiles >= (kn.wide > 1 ? 1 : dev.sm_count)) {
+      wide = true;
+      BN = (int)(((M + mt - 1) / mt + 63) / 64 * 64);
+    }
+  }
+  const int HB = wide ? BN / 2 : BN;
 
   GemmParams p = {};
   p.M = (int)M;
   p.NB = (int)(K / QK);
   p.BN = BN;
+  p.HB = HB;
   p.m_tiles = (int)((M + BN - 1) / BN);
   const int kst = atmem ? Cfg<false, true>::KST : KSTEP;  // K per pipeline step
   p.KS = (QK / kst) * p.NB;
@@ -956,10 +1058,11 @@ cudaError_t launch_tc_common(const void* const* w, const void* w1, const int64_t
 
   // Shared memory: X ring, dequantised-A ring (not with A in tensor memory),
   // raw-W ring, barriers.
-  const int SX = swiglu ? Cfg<true>::SX : (atmem ? Cfg<false, true>::SX : Cfg<false>::SX);
-  const int SA = swiglu ? Cfg<true>::SA : (atmem ? Cfg<false, true>::SA : Cfg<false>::SA);
-  const int SW = swiglu ? Cfg<true>::SW : (atmem ? Cfg<false, true>::SW : Cfg<false>::SW);
-  const int nbars = swiglu ? Cfg<true>::NBARS : (atmem ? Cfg<false, true>::NBARS : Cfg<false>::NBARS);
+  const int SX = swiglu ? Cfg<true>::SX : (atmem ? Cfg<false, true>::SX : (wide ? CW::SX : Cfg<false>::SX));
+  const int SA = swiglu ? Cfg<true>::SA : (atmem ? Cfg<false, true>::SA : (wide ? CW::SA : Cfg<false>::SA));
+  const int SW = swiglu ? Cfg<true>::SW : (atmem ? Cfg<false, true>::SW : (wide ? CW::SW : Cfg<false>::SW));
+  const int nbars =
+      swiglu ? Cfg<true>::NBARS : (atmem ? Cfg<false, true>::NBARS : (wide ? CW::NBARS : Cfg<false>::NBARS));
   p.x_stage_bytes = (uint32_t)BN * kst * 2;
   p.off_x = 0;
   p.off_a = (uint32_t)SX * p.x_stage_bytes;
@@ -971,11 +1074,12 @@ cudaError_t launch_tc_common(const void* const* w, const void* w1, const int64_t
   CUtensorMap mx;
   WMaps mw;
   memset(&mw, 0, sizeof(mw));
-  cudaError_t e = make_x_map(x, M, K, BN, &mx);
+  cudaError_t e = make_x_map(x, M, K, HB, &mx);
   for (int b = 0; b < count && e == cudaSuccess; ++b) e = make_w_map(w[b], Ns[b], K, &mw.w[b]);
   if (e == cudaSuccess && swiglu) e = make_w_map(w1, Ns[0], K, &mw.w[1]);
   if (e != cudaSuccess) return e;
   if (swiglu) return launch_tc<true, false>(mx, mw, p, grid, split, smem, s);
+  if (wide) return launch_tc<false, false, true>(mx, mw, p, grid, split, smem, s);
   return atmem ? launch_tc<false, true>(mx, mw, p, grid, split, smem, s)
                : launch_tc<false, false>(mx, mw, p, grid, split, smem, s);
 }

@@ -265,7 +265,7 @@ jllm_status jllm_q4k_gemm(const void* w_q4k, const void* x, void* y, jllm_dtype 
  * jllm_q4k_gemm_noalloc -- jllm_q4k_gemm with the library's own workspace.
  * The pages describe no such call; it exists for callers that cannot hand
  * the library device memory.  The workspace is a static device array in
- * the library image (zero at load, ~21 MB, enough for up to 160 SMs),
+ * the library image (zero at load, ~42 MB, enough for up to 160 SMs),
  * found with cudaGetSymbolAddress once per device; nothing is allocated.
  * Arguments and results as jllm_q4k_gemm without ws/ws_bytes.  The array
  * is shared by every call on a device, so calls must not overlap: issue

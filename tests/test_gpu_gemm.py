@@ -23,8 +23,11 @@ def _gemm(q, w_np, x_np, N, K, f16):
     return out.float().cpu().numpy()
 
 
-# 129..256 with few weight-row tiles also covers the split into two token tiles
-@pytest.mark.parametrize("M", [2, 5, 16, 17, 33, 64, 100, 128, 129, 130, 200, 255, 256, 257, 300])
+# 129..256 with few weight-row tiles also covers the split into two token tiles;
+# above 256 the wide tiles: one of 320 / 384 / 512 tokens (halves of 160..256,
+# the second half cut short at 449 and 511), then two, three token tiles
+@pytest.mark.parametrize("M", [2, 5, 16, 17, 33, 64, 100, 128, 129, 130, 200, 255, 256, 257, 300,
+                               384, 449, 511, 512, 513, 700, 1025])
 def test_gemm_small_full(q, M):
     N, K = 200, 768
     w = synthetic.q4k_weights(N, K, 900 + M)

@@ -33,6 +33,7 @@ CASES = [
     ([1024, 256, 256], 2560, 235),
     ([96, 1000, 130, 512], 1280, 300),
     ([128], 512, 17),
+    ([200, 72, 384], 768, 600),  # tiles of more than 256 tokens (two of 320)
 ]
 
 
@@ -57,7 +58,7 @@ def test_batch_matches_oracle_and_single_calls(q, Ns, K, M):
         assert torch.equal(split[i], again[i]), f"batch[{i}] not deterministic"
     if ws is not None:
         sms = _sms()
-        assert int(ws[sms * 131072: sms * 131072 + 4 * sms].count_nonzero()) == 0
+        assert int(ws[sms * 262144: sms * 262144 + 4 * sms].count_nonzero()) == 0
     assert q.jllm_get_device_error() == 0
 
 

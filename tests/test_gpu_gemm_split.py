@@ -26,7 +26,8 @@ def _sms():
 
 # (N, K, M): tile counts that do not fill the SMs evenly, so K ranges are cut
 # between CTAs -- a tile over several CTAs (few tiles), ragged M and N tails.
-SHAPES = [(1024, 2560, 33), (1280, 4096, 256), (200, 768, 70), (2560, 9728, 40), (300, 1280, 300), (4096, 2560, 235)]
+SHAPES = [(1024, 2560, 33), (1280, 4096, 256), (200, 768, 70), (2560, 9728, 40), (300, 1280, 300), (4096, 2560, 235),
+          (1280, 4096, 600), (520, 2816, 1025)]  # wide tiles (> 256 tokens): a tile over ~8 CTAs; three token tiles
 
 
 @pytest.mark.parametrize("N,K,M", SHAPES)
@@ -48,9 +49,9 @@ def test_split_matches_oracle_and_whole_tiles(q, N, K, M):
     # deterministic: the same call again gives the same bits
     y_again = q.jllm_q4k_gemm(wd, xd, N, K, out_dtype=torch.float32, ws=ws)
     assert torch.equal(y_split, y_again)
-    # the flag words (after one 128 KiB slot per SM) are back to zero
+    # the flag words (after one 256 KiB slot per SM) are back to zero
     sms = _sms()
-    flags = ws[sms * 131072: sms * 131072 + 4 * sms]
+    flags = ws[sms * 262144: sms * 262144 + 4 * sms]
     assert int(flags.count_nonzero()) == 0
     assert q.jllm_get_device_error() == 0
 
@@ -73,7 +74,7 @@ def test_split_swiglu(q, M):
     h2 = q.jllm_q4k_ffn_swiglu(dev(wg), dev(wu), dev(x), N, K, ws=ws).float().cpu().numpy()
     assert np.array_equal(h, h2)
     sms = _sms()
-    assert int(ws[sms * 131072: sms * 131072 + 4 * sms].count_nonzero()) == 0
+    assert int(ws[sms * 262144: sms * 262144 + 4 * sms].count_nonzero()) == 0
 
 
 def test_split_fp16_output(q):
