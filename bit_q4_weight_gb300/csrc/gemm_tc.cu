@@ -149,10 +149,14 @@ struct Cfg {
   static constexpr int SA = COMB ? SX : (SWIGLU || WIDE ? 3 : 4);  // dequantised-A ring
   static constexpr int SW = SWIGLU || WIDE ? 2 : 3;      // raw-W ring
   static constexpr int XH = WIDE ? 2 : 1;                // token halves (X boxes, MMAs) per K slice
+  // X ring slots: a stage, or (wide tiles) one token half of a stage, each with
+  // its own full / empty barrier, so that a half's MMAs start when its box has
+  // landed and its box is refilled as soon as they are done.
+  static constexpr int XS = SX * XH;
   static constexpr int NACC = WIDE ? 1 : 2;              // accumulator buffers
   static constexpr int BN_MAX = SWIGLU ? 128 : (ATMEM ? (int)ACC_COLS_ATMEM : (WIDE ? 512 : 256));
   static constexpr uint32_t ACC = ATMEM ? ACC_COLS_ATMEM : (WIDE ? TMEM_COLS : ACC_COLS);  // TMEM columns per accumulator
-  static constexpr int NBARS = 2 * (SX + SA + SW) + 2 + 2 + 1;
+  static constexpr int NBARS = 2 * (XS + SA + SW) + 2 + 2 + 1;
   static_assert(!ATMEM || (!SWIGLU && A_TMEM_COL0 + SA * ASC <= TMEM_COLS), "tensor memory budget");
   static_assert(!WIDE || (!SWIGLU && !ATMEM), "wide tiles: one plain matrix, A in shared memory");
 };
@@ -272,16 +276,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     q4k_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ WMaps tmW,
                        const __grid_constant__ GemmParams p) {
   using C = Cfg<SWIGLU, ATMEM, WIDE>;
-  constexpr int NMAT = C::NMAT, SX = C::SX, SA = C::SA, SW = C::SW;
+  constexpr int NMAT = C::NMAT, SA = C::SA, SW = C::SW, XS = C::XS;
   extern __shared__ uint8_t gemm_smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(gemm_smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   const uint32_t sx = sbase + p.off_x, sa = sbase + p.off_a, sw = sbase + p.off_w;
-  // barriers: x_full[SX] x_empty[SX] a_full[SA] a_empty[SA] w_full[SW] w_empty[SW]
+  // barriers: x_full[XS] x_empty[XS] a_full[SA] a_empty[SA] w_full[SW] w_empty[SW]
   //           (COMB: x_full / x_empty serve X and A; a_full / a_empty unused)
   //           acc_full[2] acc_empty[2] drain
-  const uint32_t b_xfull = sbase + p.off_bar, b_xempty = b_xfull + 8 * SX;
-  const uint32_t b_afull = b_xempty + 8 * SX, b_aempty = b_afull + 8 * SA;
+  const uint32_t b_xfull = sbase + p.off_bar, b_xempty = b_xfull + 8 * XS;
+  const uint32_t b_afull = b_xempty + 8 * XS, b_aempty = b_afull + 8 * SA;
+  const uint32_t x_slot_bytes = p.x_stage_bytes / C::XH;  // X ring slot: a stage or half of one
   const uint32_t b_wfull = b_aempty + 8 * SA, b_wempty = b_wfull + 8 * SW;
   const uint32_t b_accfull = b_wempty + 8 * SW, b_accempty = b_accfull + 16, b_drain = b_accempty + 16;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + p.off_bar + 8 * C::NBARS);
@@ -290,7 +295,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < SX; ++i) {
+    for (int i = 0; i < XS; ++i) {
       mbar_init(b_xfull + 8 * i, C::COMB ? 9 : 1);  // COMB: the X copy and the 8 dequant warps
       mbar_init(b_xempty + 8 * i, 1);
     }
@@ -336,40 +341,40 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // held back by the X ring.
     if (lane == 0) {
       tma_prefetch_desc(&tmX);
-      Ring<SX> rx;
+      Ring<XS> rx;
       long long nx = 0;
       bool ok = true;
       UnitIter it{u_begin, u_end, p.KS};
       while (ok && it.next()) {
         const int m0 = locate(p, it.tile).m0;
-        for (int k = it.k0; k < it.k1; ++k) {
-          if (!wait(b_xempty + 8 * rx.s, rx.ph ^ 1u)) {
-            ok = false;
-            break;
-          }
-          if (nx == 0) pdl_wait();  // X may come from the previous kernel; the weights do not
+        for (int k = it.k0; k < it.k1 && ok; ++k) {
+#pragma unroll
+          for (int t = 0; t < C::XH; ++t) {  // the slots (token halves) of the step
+            if (!wait(b_xempty + 8 * rx.s, rx.ph ^ 1u)) {
+              ok = false;
+              break;
+            }
+            if (nx == 0) pdl_wait();  // X may come from the previous kernel; the weights do not
 #ifdef JLLM_FAULT_INJECTION
-          if (!(nx == 0 && blockIdx.x == 0 && g_fi_skip_x))
+            if (!(nx == 0 && blockIdx.x == 0 && g_fi_skip_x))
 #endif
-          {
-            mbar_arrive_expect_tx(b_xfull + 8 * rx.s, p.x_stage_bytes);
-            // one box of 64 k (the 128-byte swizzle atom) x HB tokens per K half
-            // and token half of the step
+            {
+              mbar_arrive_expect_tx(b_xfull + 8 * rx.s, x_slot_bytes);
+              // one box of 64 k (the 128-byte swizzle atom) x HB tokens per K half
 #pragma unroll
-            for (int h = 0; h < C::KST / KSTEP; ++h)
-#pragma unroll
-              for (int t = 0; t < C::XH; ++t)
-                tma_load_2d(sx + (uint32_t)rx.s * p.x_stage_bytes + (uint32_t)((h * C::XH + t) * p.HB * KSTEP * 2),
-                            &tmX, b_xfull + 8 * rx.s, k * C::KST + h * KSTEP, m0 + t * p.HB);
+              for (int h = 0; h < C::KST / KSTEP; ++h)
+                tma_load_2d(sx + (uint32_t)rx.s * x_slot_bytes + (uint32_t)(h * p.HB * KSTEP * 2), &tmX,
+                            b_xfull + 8 * rx.s, k * C::KST + h * KSTEP, m0 + t * p.HB);
+            }
+            rx.next();
+            ++nx;
           }
-          rx.next();
-          ++nx;
         }
       }
       if (!ok) fail();
       // Every copy this thread issued must have landed before the CTA exits.
-      for (long long i = nx > SX ? nx - SX : 0; i < nx; ++i)
-        mbar_wait_bounded(b_xfull + 8 * (int)(i % SX), (uint32_t)((i / SX) & 1), nullptr, WAIT_LIMIT_NS);
+      for (long long i = nx > XS ? nx - XS : 0; i < nx; ++i)
+        mbar_wait_bounded(b_xfull + 8 * (int)(i % XS), (uint32_t)((i / XS) & 1), nullptr, WAIT_LIMIT_NS);
     } else if (lane == 1) {
       for (int i = 0; i < (SWIGLU ? 2 : p.count); ++i) tma_prefetch_desc(&tmW.w[i]);
       Ring<SW> rw;
@@ -408,11 +413,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // k's MMAs are issued so that the probe's latency overlaps the issue.
       const uint32_t idesc = umma_idesc_f16(TILE_N, p.HB);
       const uint64_t adesc0 = umma_desc_sw128(sa), bdesc0 = umma_desc_sw128(sx);
-      const uint32_t a_step = (uint32_t)(NMAT * A_STAGE_BYTES) >> 4, b_step = p.x_stage_bytes >> 4;
+      const uint32_t a_step = (uint32_t)(NMAT * A_STAGE_BYTES) >> 4, b_step = x_slot_bytes >> 4;
       constexpr uint32_t A2 = (uint32_t)A_STAGE_BYTES >> 4;  // second matrix of a SwiGLU stage
-      const uint32_t xhalf = (uint32_t)(p.HB * KSTEP * 2) >> 4;  // second token half of a wide X stage
       Ring<SA> ra;
-      Ring<SX> rx;
+      Ring<XS> rx;
       Ring<C::NACC> racc;
       bool ok = true;
       UnitIter it{u_begin, u_end, p.KS};
@@ -427,6 +431,36 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         bool x_ready = mbar_test_wait(b_xfull + 8 * rx.s, rx.ph);
         bool a_ready = C::COMB || mbar_test_wait(b_afull + 8 * ra.s, ra.ph);
         for (int k = it.k0; k < it.k1; ++k) {
+          if constexpr (WIDE) {
+            // The A stage, then each token half's X slot in turn: a half's four
+            // MMAs go out when its box has landed, and its slot is released
+            // (commit) as soon as they are done; the A stage after both.
+            if (!wait(b_afull + 8 * ra.s, ra.ph)) {
+              ok = false;
+              break;
+            }
+            const uint64_t ad = adesc0 + (uint64_t)(ra.s * a_step);
+            const uint32_t sa_now = ra.s;
+            ra.next();
+            const uint32_t acc0 = k > it.k0 ? 1u : 0u;
+#pragma unroll
+            for (int t = 0; t < C::XH; ++t) {
+              if (!wait(b_xfull + 8 * rx.s, rx.ph) || (t == 1 && k == it.k0 && !wait(b_accempty + 8, racc.ph ^ 1u))) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint64_t bt = bdesc0 + (uint64_t)(rx.s * b_step);
+              const uint32_t dt = d + 256u * t;
+#pragma unroll
+              for (int kk = 0; kk < KSTEP / 16; ++kk) umma_f16(dt, ad + 2 * kk, bt + 2 * kk, idesc, kk ? 1u : acc0);
+              umma_commit(b_xempty + 8 * rx.s);
+              rx.next();
+            }
+            if (!ok) break;
+            umma_commit(b_aempty + 8 * sa_now);
+            continue;
+          }
           if ((!x_ready && !wait(b_xfull + 8 * rx.s, rx.ph)) || (!a_ready && !wait(b_afull + 8 * ra.s, ra.ph))) {
             ok = false;
             break;
@@ -448,24 +482,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int kk = 0; kk < C::KST / 16; ++kk)
               umma_f16_ta(d, at + 8 * kk, bd + (kk >> 2) * half + 2 * (kk & 3), idesc, kk ? 1u : acc0);
           } else {
+            umma_f16(d, ad, bd, idesc, acc0);
+            if (SWIGLU) umma_f16(d + 128, ad + A2, bd, idesc, acc0);
 #pragma unroll
-            for (int t = 0; t < C::XH; ++t) {
-              if (WIDE && t == 1 && k == it.k0 && !wait(b_accempty + 8, racc.ph ^ 1u)) {
-                ok = false;
-                break;
-              }
-              if (WIDE && t == 1 && k == it.k0) tc_fence_after();
-              const uint32_t dt = d + 256u * t;
-              const uint64_t bt = bd + t * xhalf;
-              umma_f16(dt, ad, bt, idesc, acc0);
-              if (SWIGLU) umma_f16(dt + 128, ad + A2, bt, idesc, acc0);
-#pragma unroll
-              for (int kk = 1; kk < KSTEP / 16; ++kk) {
-                umma_f16(dt, ad + 2 * kk, bt + 2 * kk, idesc, 1u);
-                if (SWIGLU) umma_f16(dt + 128, ad + A2 + 2 * kk, bt + 2 * kk, idesc, 1u);
-              }
+            for (int kk = 1; kk < KSTEP / 16; ++kk) {
+              umma_f16(d, ad + 2 * kk, bd + 2 * kk, idesc, 1u);
+              if (SWIGLU) umma_f16(d + 128, ad + A2 + 2 * kk, bd + 2 * kk, idesc, 1u);
             }
-            if (!ok) break;
           }
           if (!C::COMB) umma_commit(b_aempty + 8 * sa_now);
           umma_commit(b_xempty + 8 * sx_now);
