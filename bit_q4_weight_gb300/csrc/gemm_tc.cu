@@ -86,6 +86,35 @@ __device__ __forceinline__ uint32_t dq_pair(uint32_t h2, uint32_t scv, uint32_t 
   return out;
 }
 
+// Cluster split-K: remote arrive on the same barrier in another CTA of the
+// cluster, a bounded wait that acquires at cluster scope, and a load from
+// another CTA's shared memory.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 0;; ++it) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    if ((it & 63u) == 63u && globaltimer_ns() - t0 > limit_ns) return false;
+  }
+}
+__device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t cluster_addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(cluster_addr)
+               : "memory");
+  return v;
+}
+
 __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
   uint32_t v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -156,7 +185,7 @@ struct Cfg {
   static constexpr int NACC = WIDE ? 1 : 2;              // accumulator buffers
   static constexpr int BN_MAX = SWIGLU ? 128 : (ATMEM ? (int)ACC_COLS_ATMEM : (WIDE ? 512 : 256));
   static constexpr uint32_t ACC = ATMEM ? ACC_COLS_ATMEM : (WIDE ? TMEM_COLS : ACC_COLS);  // TMEM columns per accumulator
-  static constexpr int NBARS = 2 * (XS + SA + SW) + 2 + 2 + 1;
+  static constexpr int NBARS = 2 * (XS + SA + SW) + 2 + 2 + 1 + 1;
   static_assert(!ATMEM || (!SWIGLU && A_TMEM_COL0 + SA * ASC <= TMEM_COLS), "tensor memory budget");
   static_assert(!WIDE || (!SWIGLU && !ATMEM), "wide tiles: one plain matrix, A in shared memory");
 };
@@ -182,6 +211,7 @@ struct GemmParams {
   uint32_t x_stage_bytes;
   uint32_t off_x, off_a, off_w, off_bar;
   int out_f16;
+  int csk;               // cluster split-K: CTAs per tile (a cluster), 0 = ranges over the tile list
 };
 
 // Stage index and phase parity of a ring of S stages.
@@ -283,12 +313,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t sx = sbase + p.off_x, sa = sbase + p.off_a, sw = sbase + p.off_w;
   // barriers: x_full[XS] x_empty[XS] a_full[SA] a_empty[SA] w_full[SW] w_empty[SW]
   //           (COMB: x_full / x_empty serve X and A; a_full / a_empty unused)
-  //           acc_full[2] acc_empty[2] drain
+  //           acc_full[2] acc_empty[2] drain cluster_ready
   const uint32_t b_xfull = sbase + p.off_bar, b_xempty = b_xfull + 8 * XS;
   const uint32_t b_afull = b_xempty + 8 * XS, b_aempty = b_afull + 8 * SA;
   const uint32_t x_slot_bytes = p.x_stage_bytes / C::XH;  // X ring slot: a stage or half of one
   const uint32_t b_wfull = b_aempty + 8 * SA, b_wempty = b_wfull + 8 * SW;
   const uint32_t b_accfull = b_wempty + 8 * SW, b_accempty = b_accfull + 16, b_drain = b_accempty + 16;
+  const uint32_t b_cready = b_drain + 8;  // cluster split-K: the partials of the cluster are in place
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + p.off_bar + 8 * C::NBARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -312,6 +343,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(b_accempty + 8 * i, NUM_EPI_WARPS);
     }
     mbar_init(b_drain, 1);
+    mbar_init(b_cready, (uint32_t)(p.csk > 0 ? p.csk * NUM_EPI_WARPS : 1));
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -322,8 +354,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Cluster split-K: every CTA's barriers are initialised before a peer arrives on them.
+  const bool csk = ATMEM && p.csk > 0;
+  if (csk) cluster_sync_all();
 
-  const long long u_begin = range_start(p, blockIdx.x), u_end = range_start(p, (long long)blockIdx.x + 1);
+  // This CTA's units: a range of the K steps laid out tile after tile, or, with
+  // cluster split-K, its share of one tile's K steps (rank r of s: [r*KS/s, (r+1)*KS/s)).
+  long long u_begin, u_end;
+  if (csk) {
+    const long long tile = blockIdx.x / p.csk, rank = blockIdx.x % p.csk;
+    u_begin = tile * p.KS + rank * p.KS / p.csk;
+    u_end = tile * p.KS + (rank + 1) * p.KS / p.csk;
+  } else {
+    u_begin = range_start(p, blockIdx.x);
+    u_end = range_start(p, (long long)blockIdx.x + 1);
+  }
 
   auto fail = [&]() {
     *abort_flag = 1;
@@ -610,10 +655,78 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)racc.s * C::ACC;
       const TileLoc loc = locate(p, it.tile);
       const int n = loc.n0 + r, m0 = loc.m0;
-      const bool writer = it.k0 > 0;                  // later part of a cut tile
-      const bool fixer = !writer && it.k1 < p.KS;      // first part of a cut tile
+      const bool writer = !csk && it.k0 > 0;          // later part of a cut tile
+      const bool fixer = !csk && !writer && it.k1 < p.KS;  // first part of a cut tile
       constexpr int MAT_COLS = SWIGLU ? 128 : 0;       // TMEM column offset of the second matrix
-      if (writer) {
+      if (csk) {
+        // Cluster split-K (the CTA's one unit): its fp32 partial of the tile goes
+        // to its own X ring ([column][row]; the ring is idle once the unit's MMAs
+        // are done), every CTA of the cluster is told that this warp's rows are in
+        // place, and then this CTA adds up its slice of the tile's rows -- the
+        // cluster's partials in rank (= K) order, read through distributed shared
+        // memory -- and stores that slice of Y.
+        float* part = reinterpret_cast<float*>(smem + p.off_x);
+        for (int cc = 0; cc < p.BN; cc += 32) {
+          uint32_t v[32];
+          tmem_ld32(tl + cc, v);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) part[(size_t)(cc + j) * TILE_N + r] = __uint_as_float(v[j]);
+        }
+        release(racc.s);  // (its __syncwarp orders the lanes' stores before lane 0's release-arrivals)
+        if (lane == 0)
+          for (int d = 0; d < p.csk; ++d) mbar_arrive_remote(mapa_shared(b_cready, (uint32_t)d));
+        int rok = 1;
+        if (lane == 0) rok = mbar_wait_cluster_bounded(b_cready, 0, WAIT_LIMIT_NS) ? 1 : 0;
+        ok = __shfl_sync(0xffffffffu, rok, 0) != 0;
+        __syncwarp();
+        if (!ok) break;
+        // This CTA's slice: 4-row groups [rank*32/s, (rank+1)*32/s) of all BN
+        // columns; a thread takes one (column, 4-row group) at a time, with
+        // every peer's 16 bytes loaded before the adds.
+        const int rank = (int)(blockIdx.x % (unsigned)p.csk);
+        const int g0 = rank * (TILE_N / 4) / p.csk, ng = (rank + 1) * (TILE_N / 4) / p.csk - g0;
+        const uint32_t part_u32 = smem_u32(part);
+        const int tid = (int)threadIdx.x - EPI_WARP0 * 32;  // 0..127
+        const bool vec = (loc.N & 3) == 0;                  // whole 4-row groups of Y are 16 / 8 bytes aligned
+        auto store4 = [&](int col, int row, float4 a) {
+          const int nn = loc.n0 + row, m = m0 + col;
+          if (m >= p.M) return;
+          const size_t o = (size_t)m * loc.N + nn;
+          if (vec && nn + 3 < loc.N) {
+            if (p.out_f16) {
+              const __half2 lo = __floats2half2_rn(a.x, a.y), hi = __floats2half2_rn(a.z, a.w);
+              *reinterpret_cast<uint2*>(reinterpret_cast<__half*>(loc.y) + o) =
+                  make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+            } else {
+              *reinterpret_cast<float4*>(reinterpret_cast<float*>(loc.y) + o) = a;
+            }
+          } else {
+            const float av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              if (nn + i < loc.N) {
+                if (p.out_f16) reinterpret_cast<__half*>(loc.y)[o + i] = __float2half_rn(av[i]);
+                else reinterpret_cast<float*>(loc.y)[o + i] = av[i];
+              }
+          }
+        };
+        const int items = ng * p.BN;
+        for (int e = tid; e < items; e += NUM_EPI_WARPS * 32) {
+          const int row = 4 * (g0 + e % ng), col = e / ng;  // consecutive threads: consecutive row groups
+          const uint32_t off = (uint32_t)((col * TILE_N + row) * 4);
+          float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int d0 = 0; d0 < p.csk; d0 += 4) {  // four peers' loads in flight, added in rank order
+            float4 v[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              v[i] = ld_cluster_f32x4(mapa_shared(part_u32 + off, (uint32_t)(d0 + i < p.csk ? d0 + i : d0)));
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              if (d0 + i < p.csk) a.x += v[i].x, a.y += v[i].y, a.z += v[i].z, a.w += v[i].w;
+          }
+          store4(col, row, a);
+        }
+      } else if (writer) {
         // Leave the fp32 partial in this CTA's slot, then count this warp in
         // the slot's flag.  Slot layout [column / 4][row][column % 4]: a warp
         // moves 16 bytes per row, 512 contiguous bytes per access.
@@ -767,6 +880,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
+  // Cluster split-K: no CTA leaves while its peers may still read its partial.
+  if (csk) cluster_sync_all();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
 }
@@ -885,11 +1000,13 @@ cudaError_t make_w_map(const void* w, int64_t N, int64_t K, CUtensorMap* mw) {
 //   atmem  1: the A operand in tensor memory (single-GEMM and batched launches)
 //   wide   1: tiles of up to 512 tokens when M > 256 and they fill the SMs
 //          (single-GEMM and batched); 2: whenever M > 256
+//   csk    1: cluster split-K for narrow tiles that do not fill the SMs
 struct GemmKnobs {
   int bn = 0;
   int split = 1;
   int atmem = 1;
   int wide = 1;
+  int csk = 1;
 };
 const GemmKnobs& gemm_knobs() {
   static GemmKnobs k = [] {
@@ -899,15 +1016,53 @@ const GemmKnobs& gemm_knobs() {
     if (const char* e = getenv("JLLM_GEMM_SPLIT")) v.split = atoi(e);
     if (const char* e = getenv("JLLM_GEMM_ATMEM")) v.atmem = atoi(e);
     if (const char* e = getenv("JLLM_GEMM_WIDE")) v.wide = atoi(e);
+    if (const char* e = getenv("JLLM_GEMM_CSK")) v.csk = atoi(e);
 #endif
     return v;
   }();
   return k;
 }
 
+// Clusters of `cs` CTAs of the narrow-tile kernel (cluster split-K) that can be
+// resident at once with `smem` bytes of shared memory each; cached per
+// (device, cluster size, shared memory).
+int max_active_clusters(int cs, size_t smem) {
+  struct Entry {
+    int dev, cs;
+    size_t smem;
+    int n;
+  };
+  static Entry cache[32];
+  static int used = 0;
+  static std::mutex mu;
+  const int dev = device_info().device;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < used; ++i)
+    if (cache[i].dev == dev && cache[i].cs == cs && cache[i].smem == smem) return cache[i].n;
+  auto kern = q4k_gemm_tc_kernel<false, true, false>;
+  int n = 0;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) == cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)cs);
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = (unsigned)cs;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+  }
+  cudaGetLastError();  // a refused query leaves no sticky error behind
+  if (used < 32) cache[used++] = Entry{dev, cs, smem, n};
+  return n;
+}
+
 template <bool SWIGLU, bool ATMEM, bool WIDE = false>
 cudaError_t launch_tc(const CUtensorMap& mx, const WMaps& mw, const GemmParams& p, int grid, bool cooperative,
-                      size_t smem, cudaStream_t s) {
+                      size_t smem, cudaStream_t s, int cluster = 0) {
   auto kern = q4k_gemm_tc_kernel<SWIGLU, ATMEM, WIDE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -916,8 +1071,15 @@ cudaError_t launch_tc(const CUtensorMap& mx, const WMaps& mw, const GemmParams& 
   cfg.blockDim = dim3(NUM_THREADS);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[3];
   unsigned n = 0;
+  if (cluster > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = (unsigned)cluster;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
   if (cooperative) {
     attr[n].id = cudaLaunchAttributeCooperative;
     attr[n].val.cooperative = 1;
@@ -1062,7 +1224,7 @@ cudaError_t launch_tc_common(const void* const* w, const void* w1, const int64_t
 
   // Stream-K when the tiles do not fill the SMs evenly and a workspace is
   // given; each CTA then takes at least 8 K steps.
-  const bool split = kn.split != 0 && ws != nullptr && ws_bytes >= gemm_workspace_bytes() && tiles % sms != 0;
+  bool split = kn.split != 0 && ws != nullptr && ws_bytes >= gemm_workspace_bytes() && tiles % sms != 0;
   int grid;
   if (split) {
     long long g = units / 8;
@@ -1094,6 +1256,31 @@ cudaError_t launch_tc_common(const void* const* w, const void* w1, const int64_t
   const size_t smem = 1024 + p.off_bar + 8 * nbars + 16;
   if (smem > dev.smem_optin) return cudaErrorInvalidValue;
 
+  // Cluster split-K for narrow tiles that are few next to the SMs: a cluster
+  // of s CTAs per tile, each taking 1/s of its K steps, the partials added
+  // through distributed shared memory -- no workspace, no flags, no cut-tile
+  // tail.  s is the largest of 4..8 (and at most the K steps) for which all
+  // the tiles' clusters can be resident at once.  Measured per launch (M = 33
+  // to 235): with 7 CTAs per tile (20 tiles) the launch takes 0.67-0.9x the
+  // time of the stream-K split, whose cut tiles then have ~7 contributors;
+  // with 3 per tile (40-48 tiles) it is 0.94-1.22x, so those keep stream-K.
+  int csk = 0;
+  if (atmem && kn.csk != 0 && tiles < sms) {
+    int cs = (int)(sms / tiles);
+    if (cs > 8) cs = 8;
+    if (cs > p.KS) cs = p.KS;
+    for (; cs >= 4; --cs)
+      if (max_active_clusters(cs, smem) >= tiles) break;
+    if (cs >= 4) csk = cs;
+  }
+  if (csk) {
+    p.csk = csk;
+    grid = (int)tiles * csk;
+    split = false;
+    p.partial = nullptr;
+    p.flags = nullptr;
+  }
+
   CUtensorMap mx;
   WMaps mw;
   memset(&mw, 0, sizeof(mw));
@@ -1103,7 +1290,7 @@ cudaError_t launch_tc_common(const void* const* w, const void* w1, const int64_t
   if (e != cudaSuccess) return e;
   if (swiglu) return launch_tc<true, false>(mx, mw, p, grid, split, smem, s);
   if (wide) return launch_tc<false, false, true>(mx, mw, p, grid, split, smem, s);
-  return atmem ? launch_tc<false, true>(mx, mw, p, grid, split, smem, s)
+  return atmem ? launch_tc<false, true>(mx, mw, p, grid, split, smem, s, csk)
                : launch_tc<false, false>(mx, mw, p, grid, split, smem, s);
 }
 

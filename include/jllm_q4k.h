@@ -254,7 +254,12 @@ size_t jllm_q4k_gemv_chain_sync_bytes(int n_steps);
  * accumulation in tensor memory).  With a workspace the tcgen05 kernel
  * shares the K steps of the last wave of tiles evenly among the SMs
  * (stream-K); the cut tiles' fp32 partials are added in a fixed order, so
- * results are deterministic for a given device.
+ * results are deterministic for a given device.  Tiles of at most 128
+ * tokens that number fewer than the SMs are instead split along K over a
+ * thread-block cluster of up to 8 CTAs (partials added in K order through
+ * distributed shared memory, no workspace); the split depends on the
+ * launch's tile count, so a batched call and single calls may differ in
+ * the last bits.
  * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED, UNSUPPORTED_DTYPE,
  *         WORKSPACE, CUDA.
  */

@@ -52,9 +52,12 @@ def test_batch_matches_oracle_and_single_calls(q, Ns, K, M):
         ref, s = oracle.matmul(w, x, n, K)
         assert_within(whole[i].cpu().numpy(), ref, s, f"whole batch[{i}] N={n} K={K} M={M}")
         assert_within(split[i].cpu().numpy(), ref, s, f"split batch[{i}] N={n} K={K} M={M}")
-        # whole tiles take the same K order as a single call: same bits
+        # the same sums as a single call, up to the order of the fp32 partial sums
+        # (narrow tiles that do not fill the SMs split K over a cluster, and how
+        # far depends on the launch's tile count)
         single = q.jllm_q4k_gemm(wd[i], xd, n, K, out_dtype=torch.float32, ws=False)
-        assert torch.equal(whole[i], single), f"batch[{i}] differs from the single call"
+        diff = np.abs(whole[i].cpu().numpy().astype(np.float64) - single.cpu().numpy())
+        assert np.all(diff <= 2 * oracle.tolerance(s)), f"batch[{i}] differs from the single call"
         assert torch.equal(split[i], again[i]), f"batch[{i}] not deterministic"
     if ws is not None:
         sms = _sms()
