@@ -13,6 +13,8 @@
 // vector's max |v| is a shuffle reduction within those lanes.  Each thread
 // keeps UNROLL vectors' loads in flight before it computes, over a grid of a
 // few CTAs per SM that strides through the vectors.
+#include <atomic>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -152,11 +154,26 @@ __global__ void __launch_bounds__(KV_THREADS) kv_decode_kernel(const uint2* __re
   }
 }
 
-int kv_grid(int64_t n_vec, int L) {
+// One wave: as many CTAs as can be resident at once (the kernel's occupancy,
+// queried once per kernel and device), fewer when the vectors do not need them;
+// the grid-stride loop covers the rest.  A grid of several partial waves would
+// leave the last one running with part of the SMs' warps.
+template <typename Kernel>
+int kv_grid(Kernel kern, int which, int64_t n_vec, int L) {
   const DevInfo& dev = device_info();
+  static std::atomic<int> resident[2][3][64];  // (encode/decode, L = 8/16/32, device)
+  const int li = L == 8 ? 0 : (L == 16 ? 1 : 2);
+  const int d = dev.device >= 0 && dev.device < 64 ? dev.device : 0;
+  int per_sm = resident[which][li][d].load();
+  if (per_sm == 0) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, KV_THREADS, 0) != cudaSuccess || per_sm < 1)
+      per_sm = 1;
+    cudaGetLastError();
+    resident[which][li][d].store(per_sm);
+  }
   const int64_t per_cta = (int64_t)(KV_THREADS / 32) * (32 / L) * KV_UNROLL;
   const int64_t want = (n_vec + per_cta - 1) / per_cta;
-  const int64_t cap = (int64_t)dev.sm_count * 8;
+  const int64_t cap = (int64_t)dev.sm_count * per_sm;
   return (int)(want < cap ? (want < 1 ? 1 : want) : cap);
 }
 
@@ -164,14 +181,13 @@ int kv_grid(int64_t n_vec, int L) {
 
 cudaError_t launch_kv_encode(const void* kv, int8_t* codes, void* scales, int64_t n_vec, int dim, cudaStream_t s) {
   const int L = dim / 8;
-  const int grid = kv_grid(n_vec, L);
   const uint4* in = static_cast<const uint4*>(kv);
   uint2* out = reinterpret_cast<uint2*>(codes);
   __half* sc = static_cast<__half*>(scales);
   switch (L) {
-    case 8: kv_encode_kernel<8><<<grid, KV_THREADS, 0, s>>>(in, out, sc, n_vec); break;
-    case 16: kv_encode_kernel<16><<<grid, KV_THREADS, 0, s>>>(in, out, sc, n_vec); break;
-    case 32: kv_encode_kernel<32><<<grid, KV_THREADS, 0, s>>>(in, out, sc, n_vec); break;
+    case 8: kv_encode_kernel<8><<<kv_grid(kv_encode_kernel<8>, 0, n_vec, L), KV_THREADS, 0, s>>>(in, out, sc, n_vec); break;
+    case 16: kv_encode_kernel<16><<<kv_grid(kv_encode_kernel<16>, 0, n_vec, L), KV_THREADS, 0, s>>>(in, out, sc, n_vec); break;
+    case 32: kv_encode_kernel<32><<<kv_grid(kv_encode_kernel<32>, 0, n_vec, L), KV_THREADS, 0, s>>>(in, out, sc, n_vec); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
@@ -179,14 +195,13 @@ cudaError_t launch_kv_encode(const void* kv, int8_t* codes, void* scales, int64_
 
 cudaError_t launch_kv_decode(const int8_t* codes, const void* scales, void* kv, int64_t n_vec, int dim, cudaStream_t s) {
   const int L = dim / 8;
-  const int grid = kv_grid(n_vec, L);
   const uint2* in = reinterpret_cast<const uint2*>(codes);
   const __half* sc = static_cast<const __half*>(scales);
   uint4* out = static_cast<uint4*>(kv);
   switch (L) {
-    case 8: kv_decode_kernel<8><<<grid, KV_THREADS, 0, s>>>(in, sc, out, n_vec); break;
-    case 16: kv_decode_kernel<16><<<grid, KV_THREADS, 0, s>>>(in, sc, out, n_vec); break;
-    case 32: kv_decode_kernel<32><<<grid, KV_THREADS, 0, s>>>(in, sc, out, n_vec); break;
+    case 8: kv_decode_kernel<8><<<kv_grid(kv_decode_kernel<8>, 1, n_vec, L), KV_THREADS, 0, s>>>(in, sc, out, n_vec); break;
+    case 16: kv_decode_kernel<16><<<kv_grid(kv_decode_kernel<16>, 1, n_vec, L), KV_THREADS, 0, s>>>(in, sc, out, n_vec); break;
+    case 32: kv_decode_kernel<32><<<kv_grid(kv_decode_kernel<32>, 1, n_vec, L), KV_THREADS, 0, s>>>(in, sc, out, n_vec); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
