@@ -11,12 +11,16 @@
 // tensor memory (lane = weight row, column = token, fp32).
 //
 // Persistent schedule.  One CTA per SM walks a contiguous range of "units":
-// the K steps (64 wide) of the tiles laid out tile after tile.  Without a
-// workspace a range is a whole number of tiles.  With one (stream-K), the
-// ranges are equal in K steps, so the last wave of tiles is shared out
-// evenly; a tile cut between CTAs is finished by the CTA that owns its first
-// K step, which adds the fp32 partial sums the later CTAs left in the
-// workspace, in CTA order (deterministic).
+// the K steps (64 wide, 128 with A in tensor memory) of the tiles laid out
+// tile after tile.  Without a workspace a range is a whole number of tiles.
+// With one (stream-K), the ranges are equal in K steps, so the last wave of
+// tiles is shared out evenly; a tile cut between CTAs is finished by the CTA
+// that owns its first K step, which adds the fp32 partial sums the later CTAs
+// left in the workspace, in CTA order (deterministic).  Tiles of at most 128
+// tokens that number at most a quarter of the SMs are split instead over a
+// thread-block cluster of 4-8 CTAs per tile (cluster split-K): each CTA takes
+// an equal share of the tile's K steps, and the partials are added in K order
+// through distributed shared memory.
 //
 // Roles (448 threads):
 //   warp 0      TMA producer: per K step one X tile {64 k x BN tokens},
