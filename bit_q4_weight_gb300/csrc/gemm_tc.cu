@@ -164,9 +164,13 @@ constexpr uint32_t A_TMEM_COL0 = 2 * ACC_COLS_ATMEM;  // first column of the A r
 // weight meets twice the tokens per synchronisation round.  The epilogue
 // releases the halves one at a time, and the next tile's first MMAs into half
 // 0 start while half 1 is still being drained.
+// SWIGLU: the tile's 128 rows pair 64 gate with 64 up rows (in each 32-lane
+// quarter of tensor memory, lanes 0-15 gate and 16-31 the up rows of the same
+// outputs), and the epilogue writes h = silu(g) * u for 64 outputs per tile;
+// otherwise the same kernel.
 template <bool SWIGLU, bool ATMEM = false, bool WIDE = false>
 struct Cfg {
-  static constexpr int NMAT = SWIGLU ? 2 : 1;            // weight matrices per tile
+  static constexpr int NMAT = 1;                         // raw-W / A stages per K step
   // K per pipeline step: 128 with A in tensor memory (two 64-wide X boxes and
   // eight MMAs per synchronisation round), else 64 (one 128-byte swizzle atom
   // of the A tile in shared memory).
@@ -179,19 +183,20 @@ struct Cfg {
   // Taken with A in tensor memory, where the A ring can match the X ring; with A
   // in shared memory the shorter A ring it would need costs more than it saves.
   static constexpr bool COMB = ATMEM;
-  static constexpr int SA = COMB ? SX : (SWIGLU || WIDE ? 3 : 4);  // dequantised-A ring
-  static constexpr int SW = SWIGLU || WIDE ? 2 : 3;      // raw-W ring
+  static constexpr int SA = COMB ? SX : (WIDE ? 3 : 4);  // dequantised-A ring
+  static constexpr int SW = WIDE ? 2 : 3;                // raw-W ring
   static constexpr int XH = WIDE ? 2 : 1;                // token halves (X boxes, MMAs) per K slice
   // X ring slots: a stage, or (wide tiles) one token half of a stage, each with
   // its own full / empty barrier, so that a half's MMAs start when its box has
   // landed and its box is refilled as soon as they are done.
   static constexpr int XS = SX * XH;
   static constexpr int NACC = WIDE ? 1 : 2;              // accumulator buffers
-  static constexpr int BN_MAX = SWIGLU ? 128 : (ATMEM ? (int)ACC_COLS_ATMEM : (WIDE ? 512 : 256));
+  static constexpr int BN_MAX = ATMEM ? (int)ACC_COLS_ATMEM : (WIDE ? 512 : 256);
   static constexpr uint32_t ACC = ATMEM ? ACC_COLS_ATMEM : (WIDE ? TMEM_COLS : ACC_COLS);  // TMEM columns per accumulator
   static constexpr int NBARS = 2 * (XS + SA + SW) + 2 + 2 + 1 + 1;
-  static_assert(!ATMEM || (!SWIGLU && A_TMEM_COL0 + SA * ASC <= TMEM_COLS), "tensor memory budget");
-  static_assert(!WIDE || (!SWIGLU && !ATMEM), "wide tiles: one plain matrix, A in shared memory");
+  static_assert(!ATMEM || A_TMEM_COL0 + SA * ASC <= TMEM_COLS, "tensor memory budget");
+  static_assert(!WIDE || !ATMEM, "wide tiles: A in shared memory");
+  static_assert(BN_MAX % 16 == 0, "token tiles are multiples of 16");
 };
 
 // Up to kMaxGemmBatch weight matrices that share X (and so K) run in one
@@ -216,6 +221,7 @@ struct GemmParams {
   uint32_t off_x, off_a, off_w, off_bar;
   int out_f16;
   int csk;               // cluster split-K: CTAs per tile (a cluster), 0 = ranges over the tile list
+  int pair;              // SwiGLU: a tile's 128 rows interleave 64 gate and 64 up rows, Y = silu(g)*u
 };
 
 // Stage index and phase parity of a ring of S stages.
@@ -258,7 +264,7 @@ __device__ __forceinline__ TileLoc locate(const GemmParams& p, int tile) {
     }
   const int local = tile - base;
   const int nt = local / p.m_tiles;
-  t.n0 = nt * TILE_N;
+  t.n0 = nt * (p.pair ? TILE_N / 2 : TILE_N);  // output columns: 64 per tile in SwiGLU pairs
   t.m0 = (local - nt * p.m_tiles) * p.BN;
   return t;
 }
@@ -359,7 +365,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   // Cluster split-K: every CTA's barriers are initialised before a peer arrives on them.
-  const bool csk = ATMEM && p.csk > 0;
+  const bool csk = ATMEM && !SWIGLU && p.csk > 0;
   if (csk) cluster_sync_all();
 
   // This CTA's units: a range of the K steps laid out tile after tile, or, with
@@ -441,9 +447,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             const uint32_t bar = b_wfull + 8 * rw.s;
             mbar_arrive_expect_tx(bar, W_STAGE_BYTES * NMAT);
-            tma_load_3d(sw + (uint32_t)(rw.s * NMAT) * W_STAGE_BYTES, mw, bar, 0, k / C::SPB, loc.n0);
-            if (SWIGLU)
-              tma_load_3d(sw + (uint32_t)(rw.s * NMAT + 1) * W_STAGE_BYTES, &tmW.w[1], bar, 0, k / C::SPB, loc.n0);
+            if (SWIGLU) {
+              // SwiGLU pairs: tile rows 32g..32g+15 are gate rows n0+16g.., rows
+              // 32g+16..32g+31 the up rows of the same outputs (16-row boxes), so that
+              // each TMEM lane quarter holds 16 (gate, up) row pairs, lane l and l+16.
+              const uint32_t dst = sw + (uint32_t)rw.s * W_STAGE_BYTES;
+#pragma unroll
+              for (int g = 0; g < 4; ++g) {
+                tma_load_3d(dst + (uint32_t)(32 * g) * BLOCK_BYTES, &tmW.w[0], bar, 0, k / C::SPB, loc.n0 + 16 * g);
+                tma_load_3d(dst + (uint32_t)(32 * g + 16) * BLOCK_BYTES, &tmW.w[1], bar, 0, k / C::SPB, loc.n0 + 16 * g);
+              }
+            } else {
+              tma_load_3d(sw + (uint32_t)(rw.s * NMAT) * W_STAGE_BYTES, mw, bar, 0, k / C::SPB, loc.n0);
+            }
             rw.next();
             ++nw;
           }
@@ -463,7 +479,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t idesc = umma_idesc_f16(TILE_N, p.HB);
       const uint64_t adesc0 = umma_desc_sw128(sa), bdesc0 = umma_desc_sw128(sx);
       const uint32_t a_step = (uint32_t)(NMAT * A_STAGE_BYTES) >> 4, b_step = x_slot_bytes >> 4;
-      constexpr uint32_t A2 = (uint32_t)A_STAGE_BYTES >> 4;  // second matrix of a SwiGLU stage
       Ring<SA> ra;
       Ring<XS> rx;
       Ring<C::NACC> racc;
@@ -532,12 +547,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               umma_f16_ta(d, at + 8 * kk, bd + (kk >> 2) * half + 2 * (kk & 3), idesc, kk ? 1u : acc0);
           } else {
             umma_f16(d, ad, bd, idesc, acc0);
-            if (SWIGLU) umma_f16(d + 128, ad + A2, bd, idesc, acc0);
 #pragma unroll
-            for (int kk = 1; kk < KSTEP / 16; ++kk) {
-              umma_f16(d, ad + 2 * kk, bd + 2 * kk, idesc, 1u);
-              if (SWIGLU) umma_f16(d + 128, ad + A2 + 2 * kk, bd + 2 * kk, idesc, 1u);
-            }
+            for (int kk = 1; kk < KSTEP / 16; ++kk) umma_f16(d, ad + 2 * kk, bd + 2 * kk, idesc, 1u);
           }
           if (!C::COMB) umma_commit(b_aempty + 8 * sa_now);
           umma_commit(b_xempty + 8 * sx_now);
@@ -661,7 +672,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int n = loc.n0 + r, m0 = loc.m0;
       const bool writer = !csk && it.k0 > 0;          // later part of a cut tile
       const bool fixer = !csk && !writer && it.k1 < p.KS;  // first part of a cut tile
-      constexpr int MAT_COLS = SWIGLU ? 128 : 0;       // TMEM column offset of the second matrix
       if (csk) {
         // Cluster split-K (the CTA's one unit): its fp32 partial of the tile goes
         // to its own X ring ([column][row]; the ring is idle once the unit's MMAs
@@ -735,14 +745,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // the slot's flag.  Slot layout [column / 4][row][column % 4]: a warp
         // moves 16 bytes per row, 512 contiguous bytes per access.
         float4* slot = reinterpret_cast<float4*>(p.partial + (size_t)blockIdx.x * SLOT_FLOATS) + r;
-        for (int mat = 0; mat < NMAT; ++mat) {
+        {
           for (int cc = 0; cc < p.BN; cc += 32) {
             uint32_t v[32];
-            tmem_ld32(tl + mat * MAT_COLS + tcol(cc), v);
+            tmem_ld32(tl + tcol(cc), v);
             if (WIDE && cc + 32 == p.HB) release(0);  // half 0 is in registers
 #pragma unroll
             for (int i = 0; i < 8; ++i)
-              __stcg(slot + (size_t)((mat * MAT_COLS + cc) / 4 + i) * TILE_N,
+              __stcg(slot + (size_t)(cc / 4 + i) * TILE_N,
                      make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
                                  __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3])));
           }
@@ -779,8 +789,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const bool summed = j_end > (int)blockIdx.x + 1;
         const float4* slot0 = reinterpret_cast<const float4*>(p.partial + (size_t)(blockIdx.x + 1) * SLOT_FLOATS) + r;
         constexpr size_t SLOT4 = SLOT_FLOATS / 4;
+        constexpr bool PIPE = WIDE && !SWIGLU;  // (no registers to spare with the SwiGLU pairs)
         float4 nx[8];
-        if (WIDE && summed) {
+        if (PIPE && summed) {
 #pragma unroll
           for (int i = 0; i < 8; ++i) nx[i] = __ldcg(slot0 + (size_t)i * TILE_N);
           for (int jc = blockIdx.x + 2; jc < j_end; ++jc)
@@ -797,7 +808,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           float a[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) a[j] = __uint_as_float(v[j]);
-          if (!WIDE) {
+          if (!PIPE) {
             for (int jc = blockIdx.x + 1; jc < j_end; ++jc) {
               const float4* slot = reinterpret_cast<const float4*>(p.partial + (size_t)jc * SLOT_FLOATS) +
                                    (size_t)(cc / 4) * TILE_N + r;
@@ -823,25 +834,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             }
           }
-          if (SWIGLU) {
-            tmem_ld32(tl + MAT_COLS + cc, v);
-            float u[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) u[j] = __uint_as_float(v[j]);
-            for (int jc = blockIdx.x + 1; jc < j_end; ++jc) {
-              const float4* slot = reinterpret_cast<const float4*>(p.partial + (size_t)jc * SLOT_FLOATS) +
-                                   (size_t)((MAT_COLS + cc) / 4) * TILE_N + r;
-#pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                const float4 t = __ldcg(slot + (size_t)i * TILE_N);
-                u[4 * i] += t.x, u[4 * i + 1] += t.y, u[4 * i + 2] += t.z, u[4 * i + 3] += t.w;
-              }
-            }
-#pragma unroll
-            for (int j = 0; j < 32; ++j) a[j] = a[j] / (1.0f + expf(-a[j])) * u[j];  // h = silu(g) * u
-          }
           const int jv = min(32, min(p.BN - cc, p.M - (m0 + cc)));
-          if (n < loc.N && jv > 0) {
+          if (SWIGLU) {
+            // Lane l < 16 holds gate row n0+16q+l, lane l+16 the up row of the same
+            // output.  The gate lane makes h for tokens 0..15 of the chunk, the up
+            // lane for 16..31: each sends the partner the value of the partner's
+            // token (one exchange per token) and keeps its own.
+            const int no = loc.n0 + 16 * q + (lane & 15);
+            const bool up_lane = lane >= 16;
+            __half* yp = reinterpret_cast<__half*>(loc.y) + (size_t)(m0 + cc + (up_lane ? 16 : 0)) * loc.N + no;
+            const int jmax = jv - (up_lane ? 16 : 0);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float mine = up_lane ? a[j + 16] : a[j];
+              const float o = __shfl_xor_sync(0xffffffffu, up_lane ? a[j] : a[j + 16], 16);
+              const float g = up_lane ? o : mine, u = up_lane ? mine : o;
+              if (j < jmax && no < loc.N) yp[(size_t)j * loc.N] = __float2half_rn(__fdividef(g, 1.0f + __expf(-g)) * u);
+            }
+          } else if (n < loc.N && jv > 0) {
             // Y[m0+cc+j][n] for the j in range: one pointer step of N per token, the
             // bounds tested once per chunk.
             const size_t off = (size_t)(m0 + cc) * loc.N + n;
@@ -974,9 +984,9 @@ cudaError_t make_x_map(const void* x, int64_t M, int64_t K, int BN, CUtensorMap*
 }
 
 // Byte view of a packed weight matrix: (144 bytes, super-block, row), one
-// super-block of 128 rows per load.
-cudaError_t make_w_map(const void* w, int64_t N, int64_t K, CUtensorMap* mw) {
-  const MapKey key{device_info().device, 1, w, N, K, 0};
+// super-block of box_rows rows per load (128, or 16 for the SwiGLU pairs).
+cudaError_t make_w_map(const void* w, int64_t N, int64_t K, CUtensorMap* mw, int box_rows = TILE_N) {
+  const MapKey key{device_info().device, 1, w, N, K, box_rows};
   if (map_lookup(key, mw)) return cudaSuccess;
   PFN_cuTensorMapEncodeTiled_v12000 enc;
   cudaError_t e = get_encoder(&enc);
@@ -984,7 +994,7 @@ cudaError_t make_w_map(const void* w, int64_t N, int64_t K, CUtensorMap* mw) {
   const int64_t NB = K / QK;
   const cuuint64_t wdims[3] = {(cuuint64_t)BLOCK_BYTES, (cuuint64_t)NB, (cuuint64_t)N};
   const cuuint64_t wstrides[2] = {(cuuint64_t)BLOCK_BYTES, (cuuint64_t)(NB * BLOCK_BYTES)};
-  const cuuint32_t wbox[3] = {BLOCK_BYTES, 1, TILE_N};
+  const cuuint32_t wbox[3] = {BLOCK_BYTES, 1, (cuuint32_t)box_rows};
   const cuuint32_t wes[3] = {1, 1, 1};
   if (enc(mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(w), wdims, wstrides, wbox, wes,
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -1163,14 +1173,17 @@ cudaError_t launch_tc_common(const void* const* w, const void* w1, const int64_t
                              void* const* y, bool y_f16, int64_t M, int64_t K, void* ws, size_t ws_bytes,
                              cudaStream_t s) {
   const DevInfo& dev = device_info();
+  // SwiGLU (w1 = up): one matrix of tiles whose 128 rows pair 64 gate and 64 up
+  // rows (the kernel's pair mode), so it takes the plain tile shapes.
   const bool swiglu = w1 != nullptr;
-  const int nmat = swiglu ? 2 : 1;
+  const int nmat = 1;
+  const int64_t rows_per_tile = swiglu ? TILE_N / 2 : TILE_N;  // output columns per tile
   if (count < 1 || count > kBatchMax || (swiglu && count != 1)) return cudaErrorInvalidValue;
   if (M > INT32_MAX / 2 || K / QK > INT32_MAX / 8) return cudaErrorInvalidValue;
   const GemmKnobs& kn = gemm_knobs();
   // Tokens per tile: the whole of M up to the cap (rounded up to 16), else
-  // the cap: 256, or 128 when the SwiGLU epilogue needs two accumulators.
-  int bn_cap = swiglu ? Cfg<true>::BN_MAX : Cfg<false>::BN_MAX;
+  // the cap (256).
+  int bn_cap = Cfg<false>::BN_MAX;
   if (kn.bn >= 16 && kn.bn <= bn_cap && kn.bn % 16 == 0) bn_cap = kn.bn;
   int BN = (int)((M + 15) / 16 * 16);
   if (BN > bn_cap) BN = bn_cap;
@@ -1178,14 +1191,14 @@ cudaError_t launch_tc_common(const void* const* w, const void* w1, const int64_t
   // tiles: two token tiles of half the size put twice the CTAs to work while
   // they still fit in one wave (each weight tile is then dequantised twice).
   int64_t n_tiles = 0;
-  for (int b = 0; b < count; ++b) n_tiles += Ns[b] > 0 ? (Ns[b] + TILE_N - 1) / TILE_N : 0;
+  for (int b = 0; b < count; ++b) n_tiles += Ns[b] > 0 ? (Ns[b] + rows_per_tile - 1) / rows_per_tile : 0;
   if (kn.bn == 0 && M > bn_cap / 2 && M <= bn_cap && 2 * n_tiles <= dev.sm_count)
     BN = (int)(((M + 1) / 2 + 15) / 16 * 16);
   // Tiles of at most 128 tokens keep the dequantised A operand in tensor memory
   // (9-12 % faster than in shared memory at the same tile width, measured at 128
   // and 192 tokens), with 128-wide K steps; wider tiles need all 512 columns for
   // two accumulators.
-  const bool atmem = !swiglu && kn.atmem != 0 && BN <= Cfg<false, true>::BN_MAX;
+  const bool atmem = kn.atmem != 0 && BN <= Cfg<false, true>::BN_MAX;
   // More than 256 tokens: wide tiles of up to 512 (the fewest tiles of at most
   // 512 tokens, each a multiple of 64, so that the halves are multiples of 32),
   // when there are at least as many as SMs.  Fewer would leave SMs idle or be
@@ -1193,7 +1206,7 @@ cudaError_t launch_tc_common(const void* const* w, const void* w1, const int64_t
   // contributor) costs more than the wide tile saves.
   using CW = Cfg<false, false, true>;
   bool wide = false;
-  if (!swiglu && kn.wide != 0 && kn.bn == 0 && M > 256) {
+  if (kn.wide != 0 && kn.bn == 0 && M > 256) {
     const int64_t mt = (M + CW::BN_MAX - 1) / CW::BN_MAX;
     if (mt * n_tiles >= (kn.wide > 1 ? 1 : dev.sm_count)) {
       wide = true;
@@ -1211,6 +1224,7 @@ cudaError_t launch_tc_common(const void* const* w, const void* w1, const int64_t
   const int kst = atmem ? Cfg<false, true>::KST : KSTEP;  // K per pipeline step
   p.KS = (QK / kst) * p.NB;
   p.out_f16 = (y_f16 || swiglu) ? 1 : 0;
+  p.pair = swiglu ? 1 : 0;
   p.count = count;
   long long tiles = 0;
   for (int b = 0; b < count; ++b) {
@@ -1218,7 +1232,7 @@ cudaError_t launch_tc_common(const void* const* w, const void* w1, const int64_t
     p.y[b] = y[b];
     p.N[b] = (int)Ns[b];
     p.tile0[b] = (int)tiles;
-    tiles += (long long)p.m_tiles * ((Ns[b] + TILE_N - 1) / TILE_N);
+    tiles += (long long)p.m_tiles * ((Ns[b] + rows_per_tile - 1) / rows_per_tile);
     if (tiles > INT32_MAX / 2) return cudaErrorInvalidValue;
   }
   p.tile0[count] = (int)tiles;
@@ -1247,11 +1261,10 @@ cudaError_t launch_tc_common(const void* const* w, const void* w1, const int64_t
 
   // Shared memory: X ring, dequantised-A ring (not with A in tensor memory),
   // raw-W ring, barriers.
-  const int SX = swiglu ? Cfg<true>::SX : (atmem ? Cfg<false, true>::SX : (wide ? CW::SX : Cfg<false>::SX));
-  const int SA = swiglu ? Cfg<true>::SA : (atmem ? Cfg<false, true>::SA : (wide ? CW::SA : Cfg<false>::SA));
-  const int SW = swiglu ? Cfg<true>::SW : (atmem ? Cfg<false, true>::SW : (wide ? CW::SW : Cfg<false>::SW));
-  const int nbars =
-      swiglu ? Cfg<true>::NBARS : (atmem ? Cfg<false, true>::NBARS : (wide ? CW::NBARS : Cfg<false>::NBARS));
+  const int SX = atmem ? Cfg<false, true>::SX : (wide ? CW::SX : Cfg<false>::SX);
+  const int SA = atmem ? Cfg<false, true>::SA : (wide ? CW::SA : Cfg<false>::SA);
+  const int SW = atmem ? Cfg<false, true>::SW : (wide ? CW::SW : Cfg<false>::SW);
+  const int nbars = atmem ? Cfg<false, true>::NBARS : (wide ? CW::NBARS : Cfg<false>::NBARS);
   p.x_stage_bytes = (uint32_t)BN * kst * 2;
   p.off_x = 0;
   p.off_a = (uint32_t)SX * p.x_stage_bytes;
@@ -1269,7 +1282,7 @@ cudaError_t launch_tc_common(const void* const* w, const void* w1, const int64_t
   // time of the stream-K split, whose cut tiles then have ~7 contributors;
   // with 3 per tile (40-48 tiles) it is 0.94-1.22x, so those keep stream-K.
   int csk = 0;
-  if (atmem && kn.csk != 0 && tiles < sms) {
+  if (atmem && !swiglu && kn.csk != 0 && tiles < sms) {  // (a CTA's row slice would split SwiGLU pairs)
     int cs = (int)(sms / tiles);
     if (cs > 8) cs = 8;
     if (cs > p.KS) cs = p.KS;
@@ -1289,10 +1302,14 @@ cudaError_t launch_tc_common(const void* const* w, const void* w1, const int64_t
   WMaps mw;
   memset(&mw, 0, sizeof(mw));
   cudaError_t e = make_x_map(x, M, K, HB, &mx);
-  for (int b = 0; b < count && e == cudaSuccess; ++b) e = make_w_map(w[b], Ns[b], K, &mw.w[b]);
-  if (e == cudaSuccess && swiglu) e = make_w_map(w1, Ns[0], K, &mw.w[1]);
+  for (int b = 0; b < count && e == cudaSuccess; ++b) e = make_w_map(w[b], Ns[b], K, &mw.w[b], swiglu ? 16 : TILE_N);
+  if (e == cudaSuccess && swiglu) e = make_w_map(w1, Ns[0], K, &mw.w[1], 16);
   if (e != cudaSuccess) return e;
-  if (swiglu) return launch_tc<true, false>(mx, mw, p, grid, split, smem, s);
+  if (swiglu) {
+    if (wide) return launch_tc<true, false, true>(mx, mw, p, grid, split, smem, s);
+    return atmem ? launch_tc<true, true>(mx, mw, p, grid, split, smem, s)
+                 : launch_tc<true, false>(mx, mw, p, grid, split, smem, s);
+  }
   if (wide) return launch_tc<false, false, true>(mx, mw, p, grid, split, smem, s);
   return atmem ? launch_tc<false, true>(mx, mw, p, grid, split, smem, s, csk)
                : launch_tc<false, false>(mx, mw, p, grid, split, smem, s);
