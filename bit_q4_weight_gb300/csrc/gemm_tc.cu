@@ -789,7 +789,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const bool summed = j_end > (int)blockIdx.x + 1;
         const float4* slot0 = reinterpret_cast<const float4*>(p.partial + (size_t)(blockIdx.x + 1) * SLOT_FLOATS) + r;
         constexpr size_t SLOT4 = SLOT_FLOATS / 4;
-        constexpr bool PIPE = WIDE && !SWIGLU;  // (no registers to spare with the SwiGLU pairs)
+        constexpr bool PIPE = WIDE;
         float4 nx[8];
         if (PIPE && summed) {
 #pragma unroll
@@ -1206,7 +1206,11 @@ cudaError_t launch_tc_common(const void* const* w, const void* w1, const int64_t
   // contributor) costs more than the wide tile saves.
   using CW = Cfg<false, false, true>;
   bool wide = false;
-  if (kn.wide != 0 && kn.bn == 0 && M > 256) {
+  // (Not for SwiGLU: its epilogue -- an exchange and a silu per output -- is
+  // slow enough that the single accumulator of a wide tile would wait for it;
+  // two 256-token accumulators hide it: 189.8 against 221.9 us for gate/up
+  // 2560 -> 2 x 9728 at M = 2048.)
+  if (!swiglu && kn.wide != 0 && kn.bn == 0 && M > 256) {
     const int64_t mt = (M + CW::BN_MAX - 1) / CW::BN_MAX;
     if (mt * n_tiles >= (kn.wide > 1 ? 1 : dev.sm_count)) {
       wide = true;
@@ -1305,11 +1309,9 @@ cudaError_t launch_tc_common(const void* const* w, const void* w1, const int64_t
   for (int b = 0; b < count && e == cudaSuccess; ++b) e = make_w_map(w[b], Ns[b], K, &mw.w[b], swiglu ? 16 : TILE_N);
   if (e == cudaSuccess && swiglu) e = make_w_map(w1, Ns[0], K, &mw.w[1], 16);
   if (e != cudaSuccess) return e;
-  if (swiglu) {
-    if (wide) return launch_tc<true, false, true>(mx, mw, p, grid, split, smem, s);
+  if (swiglu)
     return atmem ? launch_tc<true, true>(mx, mw, p, grid, split, smem, s)
                  : launch_tc<true, false>(mx, mw, p, grid, split, smem, s);
-  }
   if (wide) return launch_tc<false, false, true>(mx, mw, p, grid, split, smem, s);
   return atmem ? launch_tc<false, true>(mx, mw, p, grid, split, smem, s, csk)
                : launch_tc<false, false>(mx, mw, p, grid, split, smem, s);

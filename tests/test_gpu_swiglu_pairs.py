@@ -3,7 +3,8 @@
 A tile's 128 rows pair 64 gate rows with the 64 up rows of the same outputs
 (in each 32-lane quarter of tensor memory, lanes 0-15 gate and 16-31 up), so
 the launch takes the plain tile shapes: tensor-memory A for up to 128 tokens,
-256-token tiles, 512-token tiles when they fill the SMs, and the stream-K split.
+256-token tiles (two accumulators, so that the exchange and silu of the
+epilogue overlap the next tile), and the stream-K split.
 The cases cover output widths that are not a multiple of 64 (a last pair tile
 whose rows past N read as zero and are not stored), each tile shape, split and
 whole tiles, and the full-size gate/up at M = 2048 (sampled columns, every
@@ -41,7 +42,7 @@ CASES = [
     (200, 768, 33),
     (1000, 2560, 129),   # 144-token tiles
     (640, 1024, 256),    # one 256-token tile
-    (1000, 1280, 300),   # two 256-token tiles (too few pair tiles for 512)
+    (1000, 1280, 300),   # two token tiles (256 + 44)
 ]
 
 
@@ -62,8 +63,8 @@ def test_swiglu_pairs(q, N, K, M):
     assert q.jllm_get_device_error() == 0
 
 
-def test_swiglu_pairs_full_size_wide(q):
-    """gate/up 2560 -> 9728 at M = 2048: 152 pair tiles x 4 token tiles of 512."""
+def test_swiglu_pairs_full_size(q):
+    """gate/up 2560 -> 9728 at M = 2048: 152 pair tiles x 8 token tiles of 256."""
     N, K, M = 9728, 2560, 2048
     wg = synthetic.q4k_weights(N, K, synthetic.weight_seed(4, 0, 4))
     wu = synthetic.q4k_weights(N, K, synthetic.weight_seed(4, 0, 5))
