@@ -163,7 +163,28 @@ def test_tcgen05_gemm_batch_edge(q):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("M", [1, 33])
+def test_tcgen05_gemm_wide_edge(q):
+    """Tiles of 320 tokens (two MMAs of 160 per K slice into one 512-column
+    accumulator): 152 weight-row tiles of edge rows; every token of columns that
+    cover each row kind, the tile boundaries and the last rows."""
+    import torch
+
+    if torch.cuda.get_device_properties(0).multi_processor_count > 152:
+        pytest.skip("the launch takes wide tiles only with at least as many tiles as SMs")
+    N, K, M = 19456, 512, 300
+    w = edge_weights(N, K, 8700)
+    x = mixed_activations(M, K, 8800)
+    y = q.jllm_q4k_gemm(dev(w), dev(x), N, K, out_dtype=torch.float32).cpu().numpy()
+    cols = np.unique(np.concatenate([np.arange(2 * N_KINDS), np.arange(127, N, 1280), np.arange(N - 16, N)]))
+    ref, s = oracle.matmul_cols(w, x, N, K, cols)
+    assert_within(y[:, cols], ref, s, "wide tiles")
+    z = [c for c in cols if c % N_KINDS in ZERO_KINDS]
+    assert np.all(y[:, z] == 0.0)
+    assert q.jllm_get_device_error() == 0
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("M", [1, 33, 300])
 def test_swiglu_edge(q, M):
     N, K = 320, 2560
     # d, dmin below 2^-8 (the workloads' range) so that h = silu(g) * u stays within fp16
