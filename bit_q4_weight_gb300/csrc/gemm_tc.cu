@@ -839,16 +839,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // Lane l < 16 holds gate row n0+16q+l, lane l+16 the up row of the same
             // output.  The gate lane makes h for tokens 0..15 of the chunk, the up
             // lane for 16..31: each sends the partner the value of the partner's
-            // token (one exchange per token) and keeps its own.
+            // token (one exchange per token) and keeps its own.  The 16 exchanges go
+            // first, so that the silu chains of different tokens overlap.
             const int no = loc.n0 + 16 * q + (lane & 15);
             const bool up_lane = lane >= 16;
             __half* yp = reinterpret_cast<__half*>(loc.y) + (size_t)(m0 + cc + (up_lane ? 16 : 0)) * loc.N + no;
             const int jmax = jv - (up_lane ? 16 : 0);
+            float o[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) o[j] = __shfl_xor_sync(0xffffffffu, up_lane ? a[j] : a[j + 16], 16);
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               const float mine = up_lane ? a[j + 16] : a[j];
-              const float o = __shfl_xor_sync(0xffffffffu, up_lane ? a[j] : a[j + 16], 16);
-              const float g = up_lane ? o : mine, u = up_lane ? mine : o;
+              const float g = up_lane ? o[j] : mine, u = up_lane ? mine : o[j];
               if (j < jmax && no < loc.N) yp[(size_t)j * loc.N] = __float2half_rn(__fdividef(g, 1.0f + __expf(-g)) * u);
             }
           } else if (n < loc.N && jv > 0) {
