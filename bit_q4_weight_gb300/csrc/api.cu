@@ -257,6 +257,8 @@ jllm_status jllm_q4k_gemm(const void* w_q4k, const void* x, void* y, jllm_dtype 
   cudaStream_t s = (cudaStream_t)stream;
   if (M <= gemv_max_m())
     return from_cuda(jllm::launch_gemv(w_q4k, nullptr, x, y, N, K, (int)M, y_dt == JLLM_F16, s));
+  if (jllm::gemm_mma_takes(M, &N, 1))
+    return from_cuda(jllm::launch_gemm_mma(&w_q4k, &N, 1, x, &y, y_dt == JLLM_F16, M, K, s));
   return from_cuda(jllm::launch_gemm_tc(w_q4k, nullptr, x, y, y_dt == JLLM_F16, M, N, K, ws, ws_bytes, s));
 }
 
@@ -271,6 +273,8 @@ jllm_status jllm_q4k_gemm_noalloc(const void* w_q4k, const void* x, void* y, jll
   cudaStream_t s = (cudaStream_t)stream;
   if (M <= gemv_max_m())
     return from_cuda(jllm::launch_gemv(w_q4k, nullptr, x, y, N, K, (int)M, y_dt == JLLM_F16, s));
+  if (jllm::gemm_mma_takes(M, &N, 1))
+    return from_cuda(jllm::launch_gemm_mma(&w_q4k, &N, 1, x, &y, y_dt == JLLM_F16, M, K, s));
   void* ws = nullptr;
   size_t ws_bytes = 0;
   cudaError_t e = jllm::gemm_static_workspace(&ws, &ws_bytes);
@@ -307,6 +311,7 @@ jllm_status jllm_q4k_gemm_batch(const void* const* w_q4k, const void* x, void* c
     }
     return JLLM_OK;
   }
+  if (jllm::gemm_mma_takes(M, N, count)) return from_cuda(jllm::launch_gemm_mma(w_q4k, N, count, x, y, f16, M, K, s));
   return from_cuda(jllm::launch_gemm_tc_batch(w_q4k, N, count, x, y, f16, M, K, ws, ws_bytes, s));
 }
 
@@ -347,15 +352,16 @@ jllm_status jllm_kv_decode_i8(const int8_t* codes, const void* scales, void* kv,
 }
 
 jllm_status jllm_get_device_error(jllm_stream_t stream) {
-  uint32_t a = 0, b = 0, c = 0;
+  uint32_t a = 0, b = 0, c = 0, d = 0;
   cudaError_t e = jllm::read_clear_gemm_error(&a, (cudaStream_t)stream);
   if (e == cudaSuccess) e = jllm::read_clear_gemv_error(&b);
   if (e == cudaSuccess) e = jllm::read_clear_chain_error(&c);
+  if (e == cudaSuccess) e = jllm::read_clear_mma_error(&d);
   // A tcgen05 kernel that gave up may have left stream-K flags set in the
   // library's static workspace: clear them before anyone calls again.
   if (e == cudaSuccess && a) e = jllm::gemm_static_workspace_reset((cudaStream_t)stream);
   if (e != cudaSuccess) return JLLM_ERR_CUDA;
-  return (a | b | c) ? JLLM_ERR_DEVICE_TIMEOUT : JLLM_OK;
+  return (a | b | c | d) ? JLLM_ERR_DEVICE_TIMEOUT : JLLM_OK;
 }
 
 #ifdef JLLM_FAULT_INJECTION
@@ -371,6 +377,10 @@ jllm_status jllm_test_fault_injection(int gemm_skip_x, int gemv_skip_w) {
 // Test builds only: skip != 0 makes the producer of CTA 0 of the next GEMV
 // chains skip its first weight copy; 0 clears it.
 jllm_status jllm_test_fault_injection_chain(int skip) { return from_cuda(jllm::fault_injection_set_chain(skip)); }
+
+// Test builds only: skip != 0 makes CTA 0 of the next few-token (mma.sync)
+// GEMMs skip its first x copies; 0 clears it.
+jllm_status jllm_test_fault_injection_mma(int skip) { return from_cuda(jllm::fault_injection_set_mma(skip)); }
 #endif
 
 }  // extern "C"

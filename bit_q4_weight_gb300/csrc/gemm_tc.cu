@@ -1332,6 +1332,14 @@ cudaError_t launch_gemm_tc_batch(const void* const* w, const int64_t* N, int cou
   return launch_tc_common(w, nullptr, N, count, x, y, y_f16, M, K, ws, ws_bytes, s);
 }
 
+cudaError_t tma_map_x(const void* x, int64_t M, int64_t K, int box_tokens, CUtensorMap* map) {
+  return make_x_map(x, M, K, box_tokens, map);
+}
+
+cudaError_t tma_map_w(const void* w, int64_t N, int64_t K, int box_rows, CUtensorMap* map) {
+  return make_w_map(w, N, K, map, box_rows);
+}
+
 #ifdef JLLM_FAULT_INJECTION
 cudaError_t fault_injection_set_gemm(int skip_x) { return cudaMemcpyToSymbol(g_fi_skip_x, &skip_x, sizeof(int)); }
 #endif

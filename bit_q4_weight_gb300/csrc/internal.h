@@ -1,6 +1,7 @@
 // Internal launchers shared by the C ABI (api.cu) and the kernel files.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -75,6 +76,22 @@ constexpr int kMaxGemmBatch = 4;
 cudaError_t launch_gemm_tc_batch(const void* const* w, const int64_t* N, int count, const void* x, void* const* y,
                                  bool y_f16, int64_t M, int64_t K, void* ws, size_t ws_bytes, cudaStream_t s);
 
+// Warp-level tensor-core GEMM for a few tokens (gemm_mma.cu): y[b] = [M][N[b]]
+// = x W[b]^T for 1 <= M <= kGemmMmaMaxM, up to kMaxGemmBatch matrices over
+// the same x (fp32 out, y_f16: fp16).  No workspace: K is split over a
+// thread-block cluster.  gemm_mma_takes() says whether the C ABI sends a call
+// above the GEMV threshold to it (else the tcgen05 GEMM).
+constexpr int kGemmMmaMaxM = 40;
+bool gemm_mma_takes(int64_t M, const int64_t* N, int count);
+cudaError_t launch_gemm_mma(const void* const* w, const int64_t* N, int count, const void* x, void* const* y,
+                            bool y_f16, int64_t M, int64_t K, cudaStream_t s);
+
+// Tensor maps shared by the TMA kernels (cached per device and buffer):
+// x [M][K] fp16 as 64-wide boxes of box_tokens rows with the 128-byte swizzle;
+// W [N][K/256] Q4_K blocks as a byte view, one super-block of box_rows rows per box.
+cudaError_t tma_map_x(const void* x, int64_t M, int64_t K, int box_tokens, CUtensorMap* map);
+cudaError_t tma_map_w(const void* w, int64_t N, int64_t K, int box_rows, CUtensorMap* map);
+
 // FP16 <-> INT8 KV codec over n_vec vectors of dim (64, 128 or 256) values:
 // codes [n_vec][dim] int8, one fp16 power-of-two scale per vector.
 cudaError_t launch_kv_encode(const void* kv, int8_t* codes, void* scales, int64_t n_vec, int dim, cudaStream_t s);
@@ -97,6 +114,7 @@ cudaError_t gemm_static_workspace_reset(cudaStream_t s);
 cudaError_t fault_injection_set_gemm(int skip_x);
 cudaError_t fault_injection_set_gemv(int skip_w);
 cudaError_t fault_injection_set_chain(int skip);
+cudaError_t fault_injection_set_mma(int skip);
 #endif
 
 // Read and clear the device error word of the tcgen05 kernels (after
@@ -104,5 +122,6 @@ cudaError_t fault_injection_set_chain(int skip);
 cudaError_t read_clear_gemm_error(uint32_t* bits, cudaStream_t s);
 cudaError_t read_clear_gemv_error(uint32_t* bits);
 cudaError_t read_clear_chain_error(uint32_t* bits);
+cudaError_t read_clear_mma_error(uint32_t* bits);
 
 }  // namespace jllm

@@ -48,8 +48,8 @@
  * the CUDA driver's tensor-map encoder, a table of the 64 most recently used
  * encoded tensor maps (keyed by device, address, extents and tile; guarded by
  * a mutex), and the static workspace of jllm_q4k_gemm_noalloc.  Environment variables read (once per process):
- * JLLM_PDL and JLLM_GEMV_MAX_M, described below; no other setting changes
- * launch shapes or summation order.
+ * JLLM_PDL, JLLM_GEMV_MAX_M and JLLM_GEMM_MMA_MAX_M, described below; no
+ * other setting changes launch shapes or summation order.
  * The GEMV and GEMM kernels are launched with programmatic dependent launch:
  * they start fetching W while the kernel enqueued just before them on the
  * same stream is still running, and read X / write Y (and the workspace)
@@ -249,8 +249,20 @@ size_t jllm_q4k_gemv_chain_sync_bytes(int n_steps);
  *   x     : [M][K] fp16
  *   y     : [M][N], fp32 or fp16 (y_dt)
  *   ws, ws_bytes : optional workspace (see jllm_q4k_workspace_bytes)
- * M <= jllm_q4k_gemv_max_m() runs the GEMV kernel (gemm(M=1) == gemv);
- * larger M runs the TMA + tcgen05 kernel (fp16 dequantised W, fp32
+ * M <= jllm_q4k_gemv_max_m() runs the GEMV kernel (gemm(M=1) == gemv).
+ * A few tokens (M <= 24, or M <= 40 when W has at most 24 tiles of 128 rows,
+ * counted over all matrices of a batch) run the few-token kernel: warp-level
+ * tensor cores (mma.sync, fp16 operands, fp32 accumulation) on weights
+ * dequantised in registers in the factored form d*sc*q - dmin*m (the code
+ * products exact, the min term as exact fp16 hi + lo parts against hi + lo
+ * sub-block sums of x), K split over a thread-block cluster whose partials
+ * are added in a fixed order through distributed shared memory (no
+ * workspace; deterministic).  Its domain: |dmin*m| <= 65504 and every sum of
+ * x over 32 consecutive values of a super-block <= 65504 in magnitude.  The
+ * environment variable JLLM_GEMM_MMA_MAX_M (0..40, read once per process)
+ * replaces that rule: M up to its value take the few-token kernel whatever
+ * the shape, larger M the tcgen05 kernel.
+ * Larger M runs the TMA + tcgen05 kernel (fp16 dequantised W, fp32
  * accumulation in tensor memory).  With a workspace the tcgen05 kernel
  * shares the K steps of the last wave of tiles evenly among the SMs
  * (stream-K); the cut tiles' fp32 partials are added in a fixed order, so
@@ -301,9 +313,11 @@ jllm_status jllm_q4k_gemm_noalloc(const void* w_q4k, const void* x, void* y, jll
  *   ws, ws_bytes : optional workspace, sized by
  *           jllm_q4k_workspace_bytes(M, sum N[i], K)
  * The host arrays are read before the call returns.  M above the GEMV
- * threshold runs one persistent tcgen05 launch over the tiles of all
- * matrices, matrix by matrix (with a workspace the stream-K split covers
- * them all); at or below it, one GEMV launch per matrix.  Each Y_i equals
+ * threshold runs one launch over the tiles of all matrices, matrix by
+ * matrix: the few-token kernel where jllm_q4k_gemm's rule picks it for the
+ * batch's total rows, else one persistent tcgen05 launch (with a workspace
+ * the stream-K split covers them all); at or below the threshold, one GEMV
+ * launch per matrix.  Each Y_i equals
  * jllm_q4k_gemm(w_q4k[i], ...) within the matmul bound (the fp32
  * summation order of cut tiles follows the batch's split).
  * Errors: INVALID_ARG (also count outside 1..4), UNSUPPORTED_SHAPE,
@@ -369,7 +383,8 @@ size_t jllm_q4k_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
 /*
  * Largest M that jllm_q4k_gemm sends to the CUDA-core GEMV kernel (which
- * handles up to 8 tokens per launch); larger M run the tcgen05 kernel.  The
+ * handles up to 8 tokens per launch); larger M run the few-token or the
+ * tcgen05 kernel (jllm_q4k_gemm).  The
  * default (4) is the measured crossover; the environment variable
  * JLLM_GEMV_MAX_M (0..8), read once per process, overrides it.
  * jllm_q4k_ffn_swiglu uses the GEMV for M = 1 only.

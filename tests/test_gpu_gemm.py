@@ -56,10 +56,11 @@ def test_gemm_fp16_output(q):
 
 
 def test_gemm_unit_vectors_give_fp16_dequant(q):
-    """x rows = unit vectors: y = fp16(w) exactly (fp16 W tile, one product, fp32 accumulation)."""
+    """x rows = unit vectors: y = fp16(w) exactly (fp16 W tile, one product, fp32 accumulation).
+    80 tokens: the tcgen05 path (fewer tokens take the factored form of the few-token GEMM)."""
     N, K = 130, 512
     w = synthetic.q4k_weights(N, K, 1400)
-    ks = np.array([0, 1, 2, 31, 32, 33, 63, 64, 100, 127, 128, 200, 255, 256, 300, 511])
+    ks = np.array([0, 1, 2, 31, 32, 33, 63, 64, 100, 127, 128, 200, 255, 256, 300, 511] * 5)
     x = np.zeros((len(ks), K), dtype=np.float16)
     x[np.arange(len(ks)), ks] = 1.0
     W16 = oracle.dequant(w, N, K, "f16").astype(np.float32)

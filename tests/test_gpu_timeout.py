@@ -6,7 +6,8 @@ skips its first X tile, or warp 0 of CTA 0 of the GEMV skips its weight
 rows.  The wait on that copy then runs out: the kernel must set its error
 word, wind down (copies and MMAs in flight awaited, tensor memory freed) and
 return (the GEMV chain: CTA 0's producer skips its first copy, and the other
-CTAs give up waiting for CTA 0's step counter), jllm_get_device_error must report JLLM_ERR_DEVICE_TIMEOUT, and the
+CTAs give up waiting for CTA 0's step counter; the few-token GEMM: CTA 0 skips
+its first x copies), jllm_get_device_error must report JLLM_ERR_DEVICE_TIMEOUT, and the
 next calls on the same context must be correct again -- including
 jllm_q4k_gemm_noalloc, whose static workspace a timed-out call leaves with
 stale stream-K flags until jllm_get_device_error clears them.  Runs in a child
@@ -117,6 +118,28 @@ for rnd in range(2):
     assert chain() == 0 and lib.jllm_get_device_error(s) == 0
     assert within(yc.cpu().numpy()[None, :], r1, s1), "chain after a timeout"
     assert not sync.any().item()
+
+# few-token GEMM (warp-level tensor cores, cluster split-K): CTA 0 never issues
+# its first x copies; its peers in the cluster wait for its partial sums
+lib.jllm_test_fault_injection_mma.argtypes = [ctypes.c_int]
+Mm, Nm = 33, 1024
+wm = synthetic.q4k_weights(Nm, K, 9504); xm = synthetic.activations(Mm, K, 9505)
+rm, smm = oracle.matmul(wm, xm, Nm, K)
+wmd, xmd = torch.from_numpy(wm).cuda(), torch.from_numpy(xm).cuda()
+ym = torch.empty((Mm, Nm), dtype=torch.float32, device="cuda")
+few = lambda: lib.jllm_q4k_gemm(wmd.data_ptr(), xmd.data_ptr(), ym.data_ptr(), 0, Mm, Nm, K, None, 0, s)
+assert few() == 0 and lib.jllm_get_device_error(s) == 0 and within(ym.cpu().numpy(), rm, smm)
+for rnd in range(2):
+    assert lib.jllm_test_fault_injection_mma(1) == 0
+    t0 = time.time()
+    assert few() == 0
+    st_ = lib.jllm_get_device_error(s)
+    assert st_ == TIMEOUT, st_
+    assert time.time() - t0 < 5.0
+    assert lib.jllm_test_fault_injection_mma(0) == 0
+    ym.fill_(float("nan"))
+    assert few() == 0 and lib.jllm_get_device_error(s) == 0
+    assert within(ym.cpu().numpy(), rm, smm), "few-token GEMM after a timeout"
 print("ok")
 '''
 
