@@ -28,14 +28,15 @@ def q():
 
 # (N, K, M): tiles = ceil(N / 128), K steps = K / 128; s = min(8, SMs / tiles,
 # K steps) when that is at least 4 (on 152 SMs)
+# (M above 40: fewer tokens with these few row tiles take the few-token GEMM)
 CASES = [
-    (128, 512, 16),     # one tile, 4 K steps: s = 4, one step per CTA
-    (200, 1792, 33),    # 2 tiles, 14 K steps: s = 8, steps 1-2 per CTA
+    (128, 512, 41),     # one tile, 4 K steps: s = 4, one step per CTA
+    (200, 1792, 48),    # 2 tiles, 14 K steps: s = 8, steps 1-2 per CTA
     (1000, 2816, 50),   # 8 tiles (the last ragged), 22 K steps: s = 8
-    (2560, 9728, 33),   # 20 tiles, 76 K steps: s = 7, the down projection at M = 33
+    (2560, 9728, 64),   # 20 tiles, 76 K steps: s = 7, the down projection at M = 64
     (4096, 2560, 100),  # 32 tiles, 20 K steps: s = 4
     (300, 768, 128),    # 3 tiles, 6 K steps: s = 6; a full 128-token tile
-    (520, 1280, 20),    # 5 tiles, 10 K steps: s = 8, K steps not a multiple of s
+    (520, 1280, 45),    # 5 tiles, 10 K steps: s = 8, K steps not a multiple of s
 ]
 
 
@@ -64,11 +65,11 @@ def test_cluster_split(q, N, K, M, f16):
 
 
 def test_cluster_split_batch(q):
-    """A batch of three matrices at M = 33: 8 + 5 + 7 = 20 tiles, s = 7, the last
+    """A batch of three matrices at M = 56: 8 + 5 + 7 = 20 tiles, s = 7, the last
     tile of each matrix ragged."""
     import torch
 
-    Ns, K, M = [1000, 600, 840], 2560, 33
+    Ns, K, M = [1000, 600, 840], 2560, 56
     ws_np = [synthetic.q4k_weights(n, K, 5300 + i) for i, n in enumerate(Ns)]
     x = synthetic.activations(M, K, 5400, per_token_scale=True)
     ys = q.jllm_q4k_gemm_batch([dev(w) for w in ws_np], dev(x), Ns, K, out_dtype=torch.float32)

@@ -18,7 +18,8 @@ def q():
     return bit_q4_weight_gb300
 
 
-# cut tiles (stream-K active), a ragged tail, and M at the GEMV threshold
+# cut tiles (stream-K active), a ragged tail, M = 33 on 8 row tiles (the few-token GEMM,
+# which uses no workspace), and M at the GEMV threshold
 @pytest.mark.parametrize("N,K,M", [(1024, 2560, 33), (4096, 2560, 235), (300, 1280, 70), (2560, 9728, 64), (256, 512, 1)])
 def test_noalloc_matches_oracle_and_caller_workspace(q, N, K, M):
     import torch
