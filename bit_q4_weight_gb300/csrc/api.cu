@@ -77,12 +77,12 @@ jllm_status check_device() {
 
 jllm_status from_cuda(cudaError_t e) { return e == cudaSuccess ? JLLM_OK : JLLM_ERR_CUDA; }
 
-// Largest M sent to the CUDA-core GEMV (the tcgen05 GEMM takes the rest).  4
-// from the measured crossover (weight GB/s on the 2560->4096 / 2560->9728
-// shapes): the GEMV is 2-4x faster up to M = 4, level at M = 8 (M = 5..8 run
-// the 8-token kernel) and slower beyond.  JLLM_GEMV_MAX_M overrides it within
-// 0..kMaxGemvTokens.
-int g_gemv_max_m = 4;
+// Largest M sent to the CUDA-core GEMV (the few-token and tcgen05 GEMMs take the
+// rest).  1 from the measured crossover with the few-token GEMM: from two tokens
+// that kernel is faster on every layer shape (2560->6144, 4096->2560,
+// 2560->19456, 9728->2560: 1.0-2.4x at M = 2..4).  JLLM_GEMV_MAX_M overrides it
+// within 0..kMaxGemvTokens.
+int g_gemv_max_m = 1;
 std::once_flag g_thresh_once;
 
 int gemv_max_m() {

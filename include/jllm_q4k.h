@@ -385,8 +385,9 @@ size_t jllm_q4k_workspace_bytes(int64_t M, int64_t N, int64_t K);
  * Largest M that jllm_q4k_gemm sends to the CUDA-core GEMV kernel (which
  * handles up to 8 tokens per launch); larger M run the few-token or the
  * tcgen05 kernel (jllm_q4k_gemm).  The
- * default (4) is the measured crossover; the environment variable
- * JLLM_GEMV_MAX_M (0..8), read once per process, overrides it.
+ * default (1) is the measured crossover with the few-token kernel, which is
+ * faster from two tokens; the environment variable JLLM_GEMV_MAX_M (0..8),
+ * read once per process, overrides it.
  * jllm_q4k_ffn_swiglu uses the GEMV for M = 1 only.
  */
 int jllm_q4k_gemv_max_m(void);

@@ -71,8 +71,8 @@ def test_swiglu_then_down_chain(q, ffn, M):
 
 @pytest.mark.parametrize("M", [1, 3, 235])
 def test_gemm_fp16_output_feeds_next_gemm(q, M):
-    """Y1 = X W1^T (fp16 out) then Y2 = Y1 W2^T: GEMV -> GEMV (M <= the threshold) or
-    tcgen05 -> tcgen05."""
+    """Y1 = X W1^T (fp16 out) then Y2 = Y1 W2^T: GEMV -> GEMV (M = 1), few-token ->
+    few-token (M = 3) or tcgen05 -> tcgen05."""
     import torch
 
     K1, N1, N2 = 2560, 4096, 1024

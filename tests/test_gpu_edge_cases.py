@@ -98,44 +98,6 @@ def test_gemv_rmsnorm_batch_edge(q):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("M", [2, 3, 4])
-def test_multi_token_gemv_edge(q, M):
-    import torch
-
-    N, K = 384, 2560
-    assert M <= q.jllm_q4k_gemv_max_m()
-    w = edge_weights(N, K, 7600 + M, cap_bits=CAP_FINITE)
-    x = mixed_activations(M, K, 7700 + M)
-    y = q.jllm_q4k_gemm(dev(w), dev(x), N, K, out_dtype=torch.float32).cpu().numpy()
-    _check(y, w, x, N, K, f"multi-token gemv M={M}")
-
-
-@pytest.mark.gpu
-def test_eight_token_gemv_edge_through_threshold_override():
-    """M = 5..8 through the 8-token GEMV kernel (threshold raised in a child process)."""
-    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-    code = r'''
-import sys, numpy as np, torch
-sys.path.insert(0, sys.argv[1]); sys.path.insert(0, sys.argv[1] + "/tests")
-import bit_q4_weight_gb300 as q, oracle
-from edge_inputs import edge_weights, mixed_activations, CAP_FINITE
-assert q.jllm_q4k_gemv_max_m() == 8
-for M, N, K in ((5, 256, 2560), (8, 200, 9728)):
-    w = edge_weights(N, K, 7800 + M, cap_bits=CAP_FINITE); x = mixed_activations(M, K, 7900 + M)
-    ref, s = oracle.matmul(w, x, N, K)
-    y = q.jllm_q4k_gemm(torch.from_numpy(w).cuda(), torch.from_numpy(x).cuda(), N, K).cpu().numpy()
-    assert np.all(np.abs(y - ref) <= oracle.tolerance(s)), (M, N, K)
-    z = [n for n in range(N) if n % 8 in (1, 3)]
-    assert np.all(y[:, z] == 0.0)
-assert q.jllm_get_device_error() == 0
-print("ok")
-'''
-    env = dict(os.environ, JLLM_GEMV_MAX_M="8")
-    out = subprocess.run([sys.executable, "-c", code, root], env=env, capture_output=True, text=True, timeout=600)
-    assert out.returncode == 0 and out.stdout.strip().endswith("ok"), out.stderr[-2000:]
-
-
-@pytest.mark.gpu
 @pytest.mark.parametrize("M,split", [(48, True), (48, False), (2048, True), (235, True)])
 def test_tcgen05_gemm_edge(q, M, split):
     """The tcgen05 path (fp16 dequantised operands: d, dmin kept below 64); fewer tokens

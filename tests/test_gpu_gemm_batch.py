@@ -79,7 +79,7 @@ def test_batch_fp16_output(q):
         assert np.all(np.abs(got - ref) <= oracle.tolerance(s) + 2.0**-11 * np.abs(ref) + 2.0**-24)
 
 
-@pytest.mark.parametrize("M", [3, 4])
+@pytest.mark.parametrize("M", [1])
 def test_batch_at_or_below_threshold_runs_gemv(q, M):
     import torch
 

@@ -1,4 +1,4 @@
-"""The few-token GEMM (M <= 40): warp-level tensor cores on weights dequantised
+"""The few-token GEMM (2 <= M <= 40): warp-level tensor cores on weights dequantised
 in registers, K split over a thread-block cluster.
 
 Each CTA takes 128 weight rows and T = 8 * ceil(M / 8) tokens; the launch
@@ -34,8 +34,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 def q():
     import bit_q4_weight_gb300
 
-    if bit_q4_weight_gb300.jllm_q4k_gemv_max_m() >= 5:
-        pytest.skip("M = 5..8 run the CUDA-core GEMV under this threshold")
+    if bit_q4_weight_gb300.jllm_q4k_gemv_max_m() >= 2:
+        pytest.skip("a few tokens run the CUDA-core GEMV under this threshold")
     if os.environ.get("JLLM_GEMM_MMA_MAX_M") is not None:
         pytest.skip("the dispatch rule is overridden in this process")
     return bit_q4_weight_gb300
@@ -47,6 +47,8 @@ def _f16_tol(ref, s):
 
 # (N, K, M)
 CASES = [
+    (1000, 2560, 2),     # 8 tiles, T = 8 (2 of 8 tokens), s = 8
+    (130, 4096, 4),      # 2 tiles (the second 2 rows), s = 8 over 16 super-blocks
     (128, 2560, 5),      # one tile, T = 8, s = 8 over 10 super-blocks
     (100, 512, 8),       # one partial tile, 2 super-blocks: s = 2
     (300, 256, 16),      # 3 tiles, K = 256: no split
