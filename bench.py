@@ -476,12 +476,14 @@ def run_ours(args):
         prefill = run_prefill(torch, q, W, meta, dev, stream, args, world, tmax=tmax, sync=sync_ranks)
         if rank == 0:
             ffn = run_ffn_lmhead(torch, q, W, dev, stream, args)
+            # 33 and 235 are the short-prompt workload's sizes; 8 and 16 show the few-token GEMM
             short = {f"M{m}": run_prefill(torch, q, W, meta, dev, stream, args, world, M=m, short=True)
-                     for m in (33, 235)}
+                     for m in (8, 16, 33, 235)}
             prefill["other_M"] = {f"M{m}": run_prefill(torch, q, W, meta, dev, stream, args, world, M=m, light=True)
                                   for m in (1024, 3072)}
             short["workload"] = ("short-prompt prefill over the decode sweep's weights, per-token scaled X, "
-                                 "fp16 out, 4 launches per layer (qkv and gate/up batched)")
+                                 "fp16 out, 4 launches per layer (qkv and gate/up batched); M = 33 and 235 the "
+                                 "short-prompt sizes, M = 8 and 16 beside them")
 
     if rank == 0:
         line = {
@@ -735,8 +737,11 @@ def run_prefill(torch, q, W, meta, dev, stream, args, world, M=M_PREFILL, short=
         else:
             roof = {"bound": "tensor", "achieved": round(tf, 2), "peak": burst, "unit": "TFLOP/s",
                     "frac": round(tf / burst, 4)}
+        kern = ("q4k_gemm_mma_kernel" if M <= 24 else
+                "q4k_gemm_tc_kernel (q/k/v, gate/up) + q4k_gemm_mma_kernel (o, down)" if M <= 40 else
+                "q4k_gemm_tc_kernel")
         roof.update({"balance_point_M": round(mstar, 1), "peak_source": "measured (burst bf16; fp16 dense rate equal)",
-                     "kernel": "q4k_gemm_tc_kernel"})
+                     "kernel": kern})
         return {"M": M, "us_per_step": round(t * 1e6, 1), "weight_gbs": round(gbs, 1),
                 "tflops": round(tf, 2), "launches_per_step": layers * len(GROUPS), "roofline": roof,
                 "seven_call": {"us_per_step": round(t7 * 1e6, 1), "weight_gbs": round(wb / t7 / 1e9, 1),
