@@ -34,7 +34,7 @@
 //    accumulating straight into the total: dmin*m_j as an exact fp16 hi + lo
 //    pair against -X_j as an fp16 hi + lo pair (X_j summed in fp32 by an MMA
 //    against an indicator matrix).  Every product is exact; sums are fp32.
-//  * K order inside an MMA: lane (g, t) of a 16 x 16 x 8 step holds code
+//  * K order inside an MMA: lane (g, t) of an m16n8k16 step holds code
 //    positions 4t..4t+3 of its rows (one 32-bit word of codes per row gives
 //    four steps: two positions each of two sub-blocks), and the x fragment
 //    holds the same four positions of token g (one 64-bit shared load), so
