@@ -100,14 +100,14 @@ def test_few_token_gemm_batch(q, M):
     assert q.jllm_get_device_error() == 0
 
 
-def test_few_token_gemm_layer_shapes(q):
-    """q/k/v and gate/up batches and o, down of the layer sweep at M = 33 as
-    dispatched (o and down here, the batches on the tcgen05 kernel), fp16 out:
+@pytest.mark.parametrize("M", [8, 16, 33])
+def test_few_token_gemm_layer_shapes(q, M):
+    """q/k/v and gate/up batches and o, down of the layer sweep, as the short-prefill
+    bench launches them (at M = 33 the batches take the tcgen05 kernel), fp16 out:
     every token of sampled columns."""
     import torch
 
-    M = 33
-    rng = np.random.Generator(np.random.PCG64(33))
+    rng = np.random.Generator(np.random.PCG64(M))
     shapes = {name: (K, N, idx) for idx, (name, K, N) in enumerate(LAYER_SHAPES)}
     for group in (("q", "k", "v"), ("o",), ("gate", "up"), ("down",)):
         K = shapes[group[0]][0]
