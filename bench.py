@@ -650,8 +650,17 @@ def run_ffn_lmhead(torch, q, W, dev, stream, args):
         t = time_graph(torch, g, stream, max(5, args.steps // 10), 3)
         del g
         flops = 2.0 * M * (2 * NF * K + K * NF + NL * K)
-        out[f"M{M}"] = {"us_per_step": round(t * 1e6, 1), "weight_gbs": round(wbytes / t / 1e9, 1),
-                        "tflops": round(flops / t / 1e12, 2), "launches_per_step": 3}
+        pk = load_peaks()
+        hbm, burst = pk.get("hbm_gbs", 6800.0), pk.get("bf16_tflops", 1900.0)
+        gbs, tf = wbytes / t / 1e9, flops / t / 1e12
+        # M = 1 streams the weights (HBM-bound); M = 512 is far above the balance point
+        roof = ({"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s", "frac": round(gbs / hbm, 4),
+                 "kernel": "q4k_gemv_kernel"} if M == 1 else
+                {"bound": "tensor", "achieved": round(tf, 2), "peak": burst, "unit": "TFLOP/s",
+                 "frac": round(tf / burst, 4), "kernel": "q4k_gemm_tc_kernel",
+                 "peak_source": "measured bf16 burst (fp16 dense rate equal)"})
+        out[f"M{M}"] = {"us_per_step": round(t * 1e6, 1), "weight_gbs": round(gbs, 1),
+                        "tflops": round(tf, 2), "launches_per_step": 3, "roofline": roof}
         if M == 1:
             # the LM head alone: one large independent GEMV launch, the kernel's sustained rate
             g = torch.cuda.CUDAGraph()
