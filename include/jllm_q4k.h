@@ -371,8 +371,10 @@ jllm_status jllm_kv_decode_i8(const int8_t* codes, const void* scales, void* kv,
 
 /*
  * Workspace bytes that gemm/ffn_swiglu can use for this shape on the current
- * device (0 = the call takes none).  Passing ws = NULL is always allowed and
- * only gives up the stream-K split.  A workspace that is given must be at
+ * device (0 = the call takes none).  It depends on M, N and K only: a GEMM
+ * that the few-token kernel takes ignores a workspace it is given, while
+ * jllm_q4k_ffn_swiglu at the same M runs the tcgen05 kernel and can use it.
+ * Passing ws = NULL is always allowed and only gives up the stream-K split.  A workspace that is given must be at
  * least this large, 256-byte aligned, and zero-filled before its first use;
  * every call that completes leaves it zero-filled where that matters, so it
  * can be reused by later calls, one call at a time (calls on different
