@@ -8,7 +8,10 @@ below 4 the launch keeps the stream-K split):
 K steps that s does not divide, s limited by a short K, one tile, ragged weight
 rows and token tails, fp32 and fp16 output, and a batch whose tiles span
 matrices.  Every element is compared with the oracle; the result does not depend
-on whether a workspace is passed (the path uses none) and repeats bit for bit."""
+on whether a workspace is passed (the path uses none) and repeats bit for bit.
+By default 5..40 tokens on few row tiles take the few-token GEMM, so these cases
+use 41..128 tokens; a child process with JLLM_GEMM_MMA_MAX_M=0 runs the split at
+5..33 tokens as well."""
 import numpy as np
 import pytest
 
@@ -77,3 +80,38 @@ def test_cluster_split_batch(q):
         ref, s = oracle.matmul(w, x, n, K)
         assert_within(y.cpu().numpy(), ref, s, f"batch matrix {i}")
     assert q.jllm_get_device_error() == 0
+
+
+CHILD = r"""
+import sys
+import numpy as np, torch
+root = sys.argv[1]
+sys.path.insert(0, root); sys.path.insert(0, root + "/tests")
+import oracle, synthetic
+import bit_q4_weight_gb300 as q
+# the tcgen05 GEMM at the few-token sizes (the cluster split for narrow tiles, A in
+# tensor memory), as JLLM_GEMM_MMA_MAX_M=0 selects it
+for N, K, M in ((128, 512, 16), (200, 1792, 33), (2560, 9728, 33), (520, 1280, 20), (1000, 2560, 5)):
+    w = synthetic.q4k_weights(N, K, 5700 + N + M)
+    x = synthetic.activations(M, K, 5800 + M, per_token_scale=True)
+    ref, s = oracle.matmul(w, x, N, K)
+    wd, xd = torch.from_numpy(w).cuda(), torch.from_numpy(x).cuda()
+    y = q.jllm_q4k_gemm(wd, xd, N, K, out_dtype=torch.float32)
+    assert torch.equal(y, q.jllm_q4k_gemm(wd, xd, N, K, out_dtype=torch.float32, ws=False)), (N, K, M)
+    assert np.all(np.abs(y.cpu().numpy().astype(np.float64) - ref) <= oracle.tolerance(s)), (N, K, M)
+assert q.jllm_get_device_error() == 0
+print("ok")
+"""
+
+
+def test_cluster_split_at_few_tokens_when_selected():
+    """JLLM_GEMM_MMA_MAX_M=0 keeps the tcgen05 GEMM for 5..40 tokens: its cluster split
+    and narrow tiles there (child process: the variable is read once per process)."""
+    import os
+    import subprocess
+    import sys
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, JLLM_GEMM_MMA_MAX_M="0")
+    out = subprocess.run([sys.executable, "-c", CHILD, root], env=env, capture_output=True, text=True, timeout=900)
+    assert out.returncode == 0 and out.stdout.strip().endswith("ok"), out.stderr[-3000:]
