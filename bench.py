@@ -747,7 +747,7 @@ def run_prefill(torch, q, W, meta, dev, stream, args, world, M=M_PREFILL, short=
             roof = {"bound": "tensor", "achieved": round(tf, 2), "peak": burst, "unit": "TFLOP/s",
                     "frac": round(tf / burst, 4)}
         kern = ("q4k_gemm_mma_kernel" if M <= 24 else
-                "q4k_gemm_tc_kernel (q/k/v, gate/up) + q4k_gemm_mma_kernel (o, down)" if M <= 40 else
+                "q4k_gemm_tc_kernel (gate/up) + q4k_gemm_mma_kernel (q/k/v, o, down)" if M <= 40 else
                 "q4k_gemm_tc_kernel")
         roof.update({"balance_point_M": round(mstar, 1), "peak_source": "measured (burst bf16; fp16 dense rate equal)",
                      "kernel": kern})

@@ -48,6 +48,8 @@
 
 #include <stdlib.h>
 
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -513,6 +515,51 @@ int forced_max_m() {
   return v;
 }
 
+// Clusters of `cs` CTAs of the NT-kernel that can be resident at once (cached per
+// device, NT and cluster size; 0 when the query fails).
+template <int NT>
+int max_clusters(int cs) {
+  struct Entry {
+    int dev, cs, n;
+  };
+  static Entry cache[16];
+  static int used = 0;
+  static std::mutex mu;
+  const int dev = device_info().device;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < used; ++i)
+    if (cache[i].dev == dev && cache[i].cs == cs) return cache[i].n;
+  auto kern = q4k_gemm_mma_kernel<NT>;
+  int n = 0;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, MmaCfg<NT>::SMEM) == cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)cs);
+    cfg.blockDim = dim3(MMA_THREADS);
+    cfg.dynamicSmemBytes = MmaCfg<NT>::SMEM;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = (unsigned)cs;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+  }
+  cudaGetLastError();  // a refused query leaves no sticky error behind
+  if (used < 16) cache[used++] = Entry{dev, cs, n};
+  return n;
+}
+
+int max_clusters_for(int NT, int cs) {
+  switch (NT) {
+    case 1: return max_clusters<1>(cs);
+    case 2: return max_clusters<2>(cs);
+    case 3: return max_clusters<3>(cs);
+    case 4: return max_clusters<4>(cs);
+    default: return max_clusters<5>(cs);
+  }
+}
+
 template <int NT>
 cudaError_t launch_mma_nt(const CUtensorMap& mx, const MmaWMaps& mw, const MmaParams& p, int grid, cudaStream_t s) {
   auto kern = q4k_gemm_mma_kernel<NT>;
@@ -551,12 +598,12 @@ bool gemm_mma_takes(int64_t M, const int64_t* N, int count) {
   if (forced >= 0) return M <= forced;
   // Measured against the tcgen05 GEMM on the layer shapes (2560 -> 6144, 4096 ->
   // 2560, 2560 -> 19456, 9728 -> 2560): faster on every shape up to 24 tokens;
-  // at 25..40 tokens only where the weights make few 128-row tiles (the
-  // tcgen05 kernel's cluster split then leaves it a long fill per launch).
+  // at 25..40 tokens where the weights make at most 64 tiles of 128 rows (q/k/v,
+  // o, down; not the 152 tiles of gate/up).
   if (M <= 24) return true;
   int64_t tiles = 0;
   for (int b = 0; b < count; ++b) tiles += (N[b] + MMA_ROWS - 1) / MMA_ROWS;
-  return tiles <= 24;
+  return tiles <= 64;
 }
 
 cudaError_t launch_gemm_mma(const void* const* w, const int64_t* N, int count, const void* x, void* const* y,
@@ -583,11 +630,18 @@ cudaError_t launch_gemm_mma(const void* const* w, const int64_t* N, int count, c
   p.M = (int)M;
   p.NB = (int)(K / QK);
   p.out_f16 = y_f16 ? 1 : 0;
-  // Split K over a cluster so that the launch has about two CTAs per SM.
+  // Split K over a cluster so that the launch has about two CTAs per SM, lowered
+  // until every cluster is resident at once (a second wave of clusters doubles a
+  // launch), then the smallest split with the same largest share of super-blocks
+  // per CTA (fewer CTAs and peers for the same critical path: 10 super-blocks
+  // over 5 CTAs rather than 2, 2, 2, 2, 1, 1 over 6).
   int split = (2 * di.sm_count + tiles / 2) / tiles;
   if (split > 8) split = 8;
   if (split > p.NB) split = p.NB;
   if (split < 1) split = 1;
+  while (split > 1 && max_clusters_for(NT, split) < tiles) --split;
+  const int share = (p.NB + split - 1) / split;
+  while (split > 1 && (p.NB + split - 2) / (split - 1) == share) --split;
   p.split = split;
   const int grid = tiles * split;
   switch (NT) {

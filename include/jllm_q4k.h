@@ -250,7 +250,7 @@ size_t jllm_q4k_gemv_chain_sync_bytes(int n_steps);
  *   y     : [M][N], fp32 or fp16 (y_dt)
  *   ws, ws_bytes : optional workspace (see jllm_q4k_workspace_bytes)
  * M <= jllm_q4k_gemv_max_m() runs the GEMV kernel (gemm(M=1) == gemv).
- * A few tokens (M <= 24, or M <= 40 when W has at most 24 tiles of 128 rows,
+ * A few tokens (M <= 24, or M <= 40 when W has at most 64 tiles of 128 rows,
  * counted over all matrices of a batch) run the few-token kernel: warp-level
  * tensor cores (mma.sync, fp16 operands, fp32 accumulation) on weights
  * dequantised in registers in the factored form d*sc*q - dmin*m (the code

@@ -4,7 +4,7 @@ in registers, K split over a thread-block cluster.
 Each CTA takes 128 weight rows and T = 8 * ceil(M / 8) tokens; the launch
 splits K into s = min(8, super-blocks, about two CTAs per SM / tiles) ranges,
 one per CTA of a cluster, and the cluster adds its partial sums in rank order.
-jllm_q4k_gemm sends M <= 24, and M <= 40 when W has at most 24 tiles of 128
+jllm_q4k_gemm sends M <= 24, and M <= 40 when W has at most 64 tiles of 128
 rows, to it (the cases below are all such calls); a child process with
 JLLM_GEMM_MMA_MAX_M=40 also sends it the large shapes.  The cases cover every
 token-tile size (T = 8 .. 40), a single row tile (s = 8), super-block counts
@@ -59,6 +59,7 @@ CASES = [
     (640, 768, 32),      # T = 32, 3 super-blocks: s = 3
     (2560, 9728, 33),    # the down projection: 20 tiles, s = 8 over 38 super-blocks, T = 40
     (3072, 2560, 40),    # 24 tiles, T = 40
+    (8064, 2560, 37),    # 63 tiles, T = 40
 ]
 
 
@@ -103,8 +104,8 @@ def test_few_token_gemm_batch(q, M):
 @pytest.mark.parametrize("M", [8, 16, 33])
 def test_few_token_gemm_layer_shapes(q, M):
     """q/k/v and gate/up batches and o, down of the layer sweep, as the short-prefill
-    bench launches them (at M = 33 the batches take the tcgen05 kernel), fp16 out:
-    every token of sampled columns."""
+    bench launches them (at M = 33 the gate/up batch takes the tcgen05 kernel), fp16
+    out: every token of sampled columns."""
     import torch
 
     rng = np.random.Generator(np.random.PCG64(M))
@@ -175,7 +176,7 @@ from gpu_helpers import oracle_matmul_rows, sample_cols
 import bit_q4_weight_gb300 as q
 rng = np.random.Generator(np.random.PCG64(77))
 # shapes the default rule sends to the tcgen05 kernel: many row tiles at 25..40 tokens
-for Ns, K, M in (([4096, 1024, 1024], 2560, 33), ([9728, 9728], 2560, 40), ([19456], 512, 25)):
+for Ns, K, M in (([4096, 4096, 1024], 2560, 33), ([9728, 9728], 2560, 40), ([19456], 512, 25)):
     ws_np = [synthetic.q4k_weights(n, K, 7700 + i + M) for i, n in enumerate(Ns)]
     x = synthetic.activations(M, K, 7800 + M, per_token_scale=True)
     ys = q.jllm_q4k_gemm_batch([torch.from_numpy(w).cuda() for w in ws_np], torch.from_numpy(x).cuda(), Ns, K,
@@ -191,7 +192,7 @@ print("ok")
 
 
 def test_few_token_gemm_forced_on_large_shapes():
-    """JLLM_GEMM_MMA_MAX_M=40: the q/k/v and gate/up batches at 33 and 40 tokens and
+    """JLLM_GEMM_MMA_MAX_M=40: batches of 72 and 152 row tiles at 33 and 40 tokens and
     152 row tiles at 25 tokens through the few-token kernel (child process)."""
     env = dict(os.environ, JLLM_GEMM_MMA_MAX_M="40")
     out = subprocess.run([sys.executable, "-c", CHILD, ROOT], env=env, capture_output=True, text=True, timeout=900)
