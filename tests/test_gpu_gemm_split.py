@@ -25,9 +25,15 @@ def _sms():
 
 
 # (N, K, M): tile counts that do not fill the SMs evenly, so K ranges are cut
-# between CTAs -- a tile over several CTAs (few tiles), ragged M and N tails.
-SHAPES = [(1024, 2560, 33), (1280, 4096, 256), (200, 768, 70), (2560, 9728, 40), (300, 1280, 300), (4096, 2560, 235),
-          (1280, 4096, 600), (520, 2816, 1025)]  # wide tiles (> 256 tokens): a tile over ~8 CTAs; three token tiles
+# between CTAs where that shortens the busiest CTA by 12 K steps or more -- a tile
+# over several CTAs (few tiles), ragged M and N tails.  Cut tiles of at most 128
+# tokens (A in tensor memory): (6144, 4096, 64) with 48 tiles of 32 steps and
+# (2560, 9728, 235) with 40 of 76 (the M = 235 down projection); of 129..256
+# tokens: (300, 1280, 300), (1280, 4096, 600), (520, 2816, 1025).  (4096, 2560,
+# 235) keeps whole tiles with a workspace (64 tiles of 20 steps); (1280, 4096,
+# 256) and (200, 768, 70) take the cluster split.
+SHAPES = [(6144, 4096, 64), (1280, 4096, 256), (200, 768, 70), (2560, 9728, 235), (300, 1280, 300), (4096, 2560, 235),
+          (1280, 4096, 600), (520, 2816, 1025)]
 
 
 @pytest.mark.parametrize("N,K,M", SHAPES)
