@@ -43,38 +43,40 @@ s = torch.cuda.current_stream().cuda_stream
 def within(y, ref, s_):
     return bool(np.all(np.abs(y.astype(np.float64) - ref) <= oracle.tolerance(s_)))
 
-# tcgen05 GEMM with the stream-K split: 16 tiles over 80 CTAs, CTA 0 finishes tile 0
-M, N, K = 235, 1024, 2560
-w = synthetic.q4k_weights(N, K, 9500); x = synthetic.activations(M, K, 9501)
-ref, sref = oracle.matmul(w, x, N, K)
-wd, xd = torch.from_numpy(w).cuda(), torch.from_numpy(x).cuda()
-y = torch.empty((M, N), dtype=torch.float32, device="cuda")
-noalloc = lambda: lib.jllm_q4k_gemm_noalloc(wd.data_ptr(), xd.data_ptr(), y.data_ptr(), 0, M, N, K, s)
-assert noalloc() == 0 and lib.jllm_get_device_error(s) == 0 and within(y.cpu().numpy(), ref, sref)
-for rnd in range(2):
-    assert lib.jllm_test_fault_injection(1, 0) == 0
-    t0 = time.time()
-    assert noalloc() == 0
-    st = lib.jllm_get_device_error(s)
-    assert st == TIMEOUT, st
-    assert time.time() - t0 < 5.0  # the kernel returned after its bounded waits
-    assert lib.jllm_test_fault_injection(0, 0) == 0
-    for _ in range(2):
-        y.fill_(float("nan"))
+# tcgen05 GEMM: 16 tiles of 128 tokens as clusters splitting K (no workspace), and
+# 20 tiles of 256 tokens of 64 K steps with the stream-K split, whose flags a timed-out
+# call leaves set (the no-alloc array: cleared by jllm_get_device_error; a caller
+# workspace: zero-filled again by its owner)
+for M, N, K in ((235, 1024, 2560), (300, 1280, 4096)):
+    w = synthetic.q4k_weights(N, K, 9500); x = synthetic.activations(M, K, 9501)
+    ref, sref = oracle.matmul(w, x, N, K)
+    wd, xd = torch.from_numpy(w).cuda(), torch.from_numpy(x).cuda()
+    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    noalloc = lambda: lib.jllm_q4k_gemm_noalloc(wd.data_ptr(), xd.data_ptr(), y.data_ptr(), 0, M, N, K, s)
+    assert noalloc() == 0 and lib.jllm_get_device_error(s) == 0 and within(y.cpu().numpy(), ref, sref)
+    for rnd in range(2):
+        assert lib.jllm_test_fault_injection(1, 0) == 0
+        t0 = time.time()
         assert noalloc() == 0
-        assert lib.jllm_get_device_error(s) == 0
-        assert within(y.cpu().numpy(), ref, sref), "noalloc after a timeout"
+        st = lib.jllm_get_device_error(s)
+        assert st == TIMEOUT, (M, st)
+        assert time.time() - t0 < 5.0  # the kernel returned after its bounded waits
+        assert lib.jllm_test_fault_injection(0, 0) == 0
+        for _ in range(2):
+            y.fill_(float("nan"))
+            assert noalloc() == 0
+            assert lib.jllm_get_device_error(s) == 0
+            assert within(y.cpu().numpy(), ref, sref), ("noalloc after a timeout", M)
+    need = lib.jllm_q4k_workspace_bytes(M, N, K)
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    gemm = lambda: lib.jllm_q4k_gemm(wd.data_ptr(), xd.data_ptr(), y.data_ptr(), 0, M, N, K, ws.data_ptr(), need, s)
+    assert lib.jllm_test_fault_injection(1, 0) == 0
+    assert gemm() == 0 and lib.jllm_get_device_error(s) == TIMEOUT
+    assert lib.jllm_test_fault_injection(0, 0) == 0
+    ws.zero_()
+    assert gemm() == 0 and lib.jllm_get_device_error(s) == 0 and within(y.cpu().numpy(), ref, sref)
 
-# the same with a caller workspace: zero-filled again by its owner after the timeout
-need = lib.jllm_q4k_workspace_bytes(M, N, K)
-ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
-gemm = lambda: lib.jllm_q4k_gemm(wd.data_ptr(), xd.data_ptr(), y.data_ptr(), 0, M, N, K, ws.data_ptr(), need, s)
-assert lib.jllm_test_fault_injection(1, 0) == 0
-assert gemm() == 0 and lib.jllm_get_device_error(s) == TIMEOUT
-assert lib.jllm_test_fault_injection(0, 0) == 0
-ws.zero_()
-assert gemm() == 0 and lib.jllm_get_device_error(s) == 0 and within(y.cpu().numpy(), ref, sref)
-
+K = 2560
 # GEMV (M = 1): warp 0 of CTA 0 never gets its rows
 N1 = 4096
 w1 = synthetic.q4k_weights(N1, K, 9502); x1 = synthetic.activations(1, K, 9503)
