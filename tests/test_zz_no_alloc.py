@@ -18,9 +18,12 @@ def q():
     return bit_q4_weight_gb300
 
 
-# cut tiles (stream-K active), a ragged tail, M = 33 on 8 row tiles (the few-token GEMM,
-# which uses no workspace), and M at the GEMV threshold
-@pytest.mark.parametrize("N,K,M", [(1024, 2560, 33), (4096, 2560, 235), (300, 1280, 70), (2560, 9728, 64), (256, 512, 1)])
+# cut tiles on the static array (stream-K: 20 tiles of 256 tokens, 64 K steps), whole
+# tiles (64 of 20 steps), the cluster split (3 and 20 narrow tiles, a ragged tail),
+# M = 33 on 8 row tiles (the few-token GEMM), and M at the GEMV threshold -- none but
+# the first touches the array, and every one must leave it reusable
+@pytest.mark.parametrize("N,K,M", [(1280, 4096, 300), (1024, 2560, 33), (4096, 2560, 235), (300, 1280, 70),
+                                   (2560, 9728, 64), (256, 512, 1)])
 def test_noalloc_matches_oracle_and_caller_workspace(q, N, K, M):
     import torch
 
