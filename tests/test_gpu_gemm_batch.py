@@ -96,15 +96,17 @@ def test_batch_at_or_below_threshold_runs_gemv(q, M):
         assert torch.equal(ys[i], q.jllm_q4k_gemm(wd[i], xd, n, K, out_dtype=torch.float32))
 
 
-@pytest.mark.parametrize("M", [33, 2048])
+@pytest.mark.parametrize("M", [33, 235, 2048])
 def test_batch_qkv_and_gate_up_layer_shapes(q, M):
-    """q/k/v (2560 -> 4096, 1024, 1024) and gate/up (2560 -> 9728 x 2) of the
-    layer sweep, as the prefill bench launches them, fp16 out, with the
-    workspace: sampled outputs against the oracle."""
+    """q/k/v (2560 -> 4096, 1024, 1024) and gate/up (2560 -> 9728 x 2) batches and
+    o (4096 -> 2560) and down (9728 -> 2560) of the layer sweep, as the prefill
+    bench launches them, fp16 out, with the workspace: sampled outputs against the
+    oracle.  At M = 235 the q/k/v batch keeps whole tiles while o and down cut
+    them (stream-K)."""
     import torch
 
     shapes = {name: (K, N, idx) for idx, (name, K, N) in enumerate(LAYER_SHAPES)}
-    for group in (("q", "k", "v"), ("gate", "up")):
+    for group in (("q", "k", "v"), ("gate", "up"), ("o",), ("down",)):
         K = shapes[group[0]][0]
         Ns = [shapes[g][1] for g in group]
         ws_np = [synthetic.q4k_weights(shapes[g][1], K, synthetic.weight_seed(3, 0, shapes[g][2])) for g in group]
