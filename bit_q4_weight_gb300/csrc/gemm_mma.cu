@@ -73,6 +73,7 @@ constexpr int MMA_CWARPS = 4;                        // consumer warps, 32 rows 
 constexpr int MMA_THREADS = (MMA_CWARPS + 1) * 32;   // + the copy / x-sum warp
 constexpr int W_STAGE = MMA_ROWS * BLOCK_BYTES;      // 18432 bytes
 constexpr int RED_PITCH = MMA_ROWS + 4;              // floats per token row of the partial sums
+constexpr int kMmaMaxSplit = 16;                     // CTAs per cluster (above 8: non-portable)
 
 template <int NT>
 struct MmaCfg {
@@ -440,10 +441,11 @@ __global__ void __launch_bounds__(MMA_THREADS, 2)
   // partials are read with 16-byte loads, all in flight before they are added.
   const int ga = rank * (MMA_ROWS / 4) / split, gb = (rank + 1) * (MMA_ROWS / 4) / split, ng = gb - ga;
   const int M = p.M;
-  uint32_t peer[8];
+  uint32_t peer[kMmaMaxSplit];
   const uint32_t red_u32 = smem_u32(smem);
 #pragma unroll
-  for (int q = 0; q < 8; ++q) peer[q] = (split > 1 && q < split) ? mapa_shared(red_u32, (uint32_t)q) : red_u32;
+  for (int q = 0; q < kMmaMaxSplit; ++q)
+    peer[q] = (split > 1 && q < split) ? mapa_shared(red_u32, (uint32_t)q) : red_u32;
   const bool vec = (N & 3) == 0;
   if (!*abort_v)
     for (int e = threadIdx.x; e < ng * M; e += MMA_THREADS) {
@@ -453,13 +455,13 @@ __global__ void __launch_bounds__(MMA_THREADS, 2)
       const uint32_t off = (uint32_t)(tk * RED_PITCH + r) * 4u;
       float4 v;
       if (split > 1) {
-        float4 part[8];
+        float4 part[kMmaMaxSplit];
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
+        for (int q = 0; q < kMmaMaxSplit; ++q)
           if (q < split) part[q] = ld_cluster_v4(peer[q] + off);
         v = part[0];
 #pragma unroll
-        for (int q = 1; q < 8; ++q)
+        for (int q = 1; q < kMmaMaxSplit; ++q)
           if (q < split) {
             v.x += part[q].x;
             v.y += part[q].y;
@@ -522,7 +524,7 @@ int max_clusters(int cs) {
   struct Entry {
     int dev, cs, n;
   };
-  static Entry cache[16];
+  static Entry cache[32];
   static int used = 0;
   static std::mutex mu;
   const int dev = device_info().device;
@@ -531,7 +533,8 @@ int max_clusters(int cs) {
     if (cache[i].dev == dev && cache[i].cs == cs) return cache[i].n;
   auto kern = q4k_gemm_mma_kernel<NT>;
   int n = 0;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, MmaCfg<NT>::SMEM) == cudaSuccess) {
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, MmaCfg<NT>::SMEM) == cudaSuccess &&
+      (cs <= 8 || cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess)) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)cs);
     cfg.blockDim = dim3(MMA_THREADS);
@@ -546,7 +549,7 @@ int max_clusters(int cs) {
     if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
   }
   cudaGetLastError();  // a refused query leaves no sticky error behind
-  if (used < 16) cache[used++] = Entry{dev, cs, n};
+  if (used < 32) cache[used++] = Entry{dev, cs, n};
   return n;
 }
 
@@ -565,6 +568,7 @@ cudaError_t launch_mma_nt(const CUtensorMap& mx, const MmaWMaps& mw, const MmaPa
   auto kern = q4k_gemm_mma_kernel<NT>;
   constexpr int smem = MmaCfg<NT>::SMEM;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess && p.split > 8) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
@@ -636,7 +640,7 @@ cudaError_t launch_gemm_mma(const void* const* w, const int64_t* N, int count, c
   // per CTA (fewer CTAs and peers for the same critical path: 10 super-blocks
   // over 5 CTAs rather than 2, 2, 2, 2, 1, 1 over 6).
   int split = (2 * di.sm_count + tiles / 2) / tiles;
-  if (split > 8) split = 8;
+  if (split > kMmaMaxSplit) split = kMmaMaxSplit;
   if (split > p.NB) split = p.NB;
   if (split < 1) split = 1;
   while (split > 1 && max_clusters_for(NT, split) < tiles) --split;
